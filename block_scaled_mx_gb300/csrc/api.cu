@@ -1,0 +1,317 @@
+// C ABI of libmxmoe.so: argument validation, workspace carving and the
+// orchestration of the MX MoE expert layer (see include/mxmoe.h).
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/mxmoe.h"
+#include "internal.h"
+
+using namespace mxk;
+
+namespace {
+
+uint64_t g_wait_limit_ns = 2000000000ull;
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline size_t al256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
+
+// Token-row tile width of the grouped GEMMs: the narrow decode schedule keeps
+// two accumulator buffers per CTA so one tile's epilogue overlaps the next
+// tile's weight stream; the wide prefill schedule reuses each weight tile over
+// 128 token rows.  Chosen from the mean rows per expert, known on the host.
+int choose_bn(int T, int E, int k) {
+  const char* env = std::getenv("MXMOE_BN");
+  if (env) {
+    const int v = std::atoi(env);
+    if (v == 32 || v == 64 || v == 128) return v;
+  }
+  const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
+  return mean_rows >= 48.0 ? 128 : 32;
+}
+
+int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k < 1 || k > E || k > 32) return MX_ERR_INVALID_ARG;
+  if (fmt != MX_E4M3 && fmt != MX_E2M1) return MX_ERR_INVALID_ARG;
+  if (H % 128 || I % 128 || E > 1024) return MX_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(T) * (k + 1) > INT32_MAX / 2) return MX_ERR_UNSUPPORTED;
+  return MX_OK;
+}
+
+// moe_forward workspace carve (status word first, shared with the permutation
+// scratch).
+struct ForwardWs {
+  PermuteScratch perm;
+  int32_t* ids;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_slot;
+  uint8_t* act_codes;
+  uint8_t* act_scales;
+  uint8_t* act_sorted;
+  uint8_t* h_codes;
+  uint8_t* h_scales;
+  size_t bytes;
+};
+
+ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
+  ForwardWs f{};
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  size_t off = 0;
+  const size_t slots = static_cast<size_t>(T) * (k + 1);
+  auto take = [&](size_t b) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += al256(b);
+    return r;
+  };
+  uint8_t* perm = take(permute_scratch_bytes(T, E, k));
+  if (p) f.perm = permute_scratch_carve(perm, T, E, k);
+  f.ids = reinterpret_cast<int32_t*>(take(static_cast<size_t>(T) * k * 4));
+  f.topk_w = reinterpret_cast<float*>(take(static_cast<size_t>(T) * k * 4));
+  f.counts = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E + 1) * 4));
+  f.offsets = reinterpret_cast<int32_t*>(take(static_cast<size_t>(E + 2) * 4));
+  f.sorted_slot = reinterpret_cast<int32_t*>(take(slots * 4));
+  f.act_codes = take(static_cast<size_t>(T) * H);
+  f.act_scales = take(static_cast<size_t>(T) * (H / 32));
+  f.act_sorted = take(slots * H);
+  f.h_codes = take(slots * I);
+  f.h_scales = take(slots * (I / 32));
+  f.bytes = off;
+  return f;
+}
+
+int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t* offsets,
+              const int32_t* sorted_slot, const void* w1_prep, int fmt, int T, int H, int I, int E,
+              int k, uint8_t* h_codes, uint8_t* h_scales, int* status, uint8_t* act_sorted,
+              cudaStream_t s) {
+  const int n_rows = T * (k + 1);
+  if (n_rows == 0) return MX_OK;
+  cudaError_t e = launch_gather_rows(act_codes, T, H, sorted_slot, k, n_rows, act_sorted, status, s);
+  if (e != cudaSuccess) return MX_ERR_CUDA;
+  GemmArgs a{};
+  a.epi = 0;
+  a.fmt = fmt;
+  a.T = T;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.k = k;
+  a.w_prep = w1_prep;
+  a.b_codes = act_sorted;
+  a.n_rows = n_rows;
+  a.b_scales = act_scales;
+  a.offsets = offsets;
+  a.sorted_slot = sorted_slot;
+  a.h_codes = h_codes;
+  a.h_scales = h_scales;
+  a.status = status;
+  a.bn = choose_bn(T, E, k);
+  a.wait_limit_ns = g_wait_limit_ns;
+  return cuda_status(launch_grouped_gemm(a, s));
+}
+
+int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* offsets,
+              const int32_t* sorted_slot, const float* topk_w, const void* w2_prep, int fmt, int T,
+              int H, int I, int E, int k, float* out, int* status, cudaStream_t s) {
+  const int n_rows = T * (k + 1);
+  if (n_rows == 0) return MX_OK;
+  GemmArgs a{};
+  a.epi = 1;
+  a.fmt = fmt;
+  a.T = T;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.k = k;
+  a.w_prep = w2_prep;
+  a.b_codes = h_codes;
+  a.n_rows = n_rows;
+  a.b_scales = h_scales;
+  a.offsets = offsets;
+  a.sorted_slot = sorted_slot;
+  a.topk_w = topk_w;
+  a.out = out;
+  a.status = status;
+  a.bn = choose_bn(T, E, k);
+  a.wait_limit_ns = g_wait_limit_ns;
+  return cuda_status(launch_grouped_gemm(a, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mx_status_string(int status) {
+  switch (status) {
+    case MX_OK: return "ok";
+    case MX_ERR_INVALID_ARG: return "invalid argument";
+    case MX_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MX_ERR_ALIGNMENT: return "pointer not sufficiently aligned";
+    case MX_ERR_WORKSPACE: return "workspace or destination too small";
+    case MX_ERR_CUDA: return "CUDA error";
+    case MX_ERR_TIMEOUT: return "device wait timed out";
+    case MX_ERR_DEVICE_ARG: return "device-side index out of range";
+    default: return "unknown status";
+  }
+}
+
+int mx_quantize_act(const void* x_bf16, int T, int H, uint8_t* codes, uint8_t* scales,
+                    mx_stream_t stream) {
+  if (T < 0 || H <= 0) return MX_ERR_INVALID_ARG;
+  if (T == 0) return MX_OK;
+  if (!x_bf16 || !codes || !scales) return MX_ERR_INVALID_ARG;
+  if (H % 32) return MX_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16)) return MX_ERR_ALIGNMENT;
+  return cuda_status(launch_quantize_act(x_bf16, static_cast<int64_t>(T) * H, codes, scales,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mx_quantize_weights(const float* w, int64_t rows, int K, int fmt, uint8_t* codes,
+                        uint8_t* scales, mx_stream_t stream) {
+  if (rows < 0 || K <= 0 || (fmt != MX_E4M3 && fmt != MX_E2M1)) return MX_ERR_INVALID_ARG;
+  if (rows == 0) return MX_OK;
+  if (!w || !codes || !scales) return MX_ERR_INVALID_ARG;
+  if (K % 32) return MX_ERR_UNSUPPORTED;
+  if (!aligned(w, 16) || !aligned(codes, 16)) return MX_ERR_ALIGNMENT;
+  return cuda_status(launch_quantize_weights(w, rows * K, fmt, codes, scales,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                   mx_stream_t stream) {
+  if (T < 0 || E <= 0 || k < 1 || k > E || k > 32) return MX_ERR_INVALID_ARG;
+  if (E > 1024) return MX_ERR_UNSUPPORTED;
+  if (T == 0) return MX_OK;
+  if (!logits || !topk_ids || !topk_w) return MX_ERR_INVALID_ARG;
+  return cuda_status(launch_topk(logits, T, E, k, topk_ids, topk_w, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_permute_workspace_size(int T, int E, int k) {
+  if (T < 0 || E <= 0 || k < 1) return 0;
+  return permute_scratch_bytes(T, E, k);
+}
+
+int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                int32_t* sorted_slot, void* ws, size_t ws_bytes, mx_stream_t stream) {
+  if (T < 0 || E <= 0 || k < 1 || k > E || k > 32) return MX_ERR_INVALID_ARG;
+  if (E > 1024) return MX_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !ws || (T > 0 && (!topk_ids || !sorted_slot))) return MX_ERR_INVALID_ARG;
+  if (ws_bytes < permute_scratch_bytes(T, E, k)) return MX_ERR_WORKSPACE;
+  if (!aligned(ws, 256)) return MX_ERR_ALIGNMENT;
+  const PermuteScratch sc = permute_scratch_carve(ws, T, E, k);
+  return cuda_status(launch_permute(topk_ids, T, E, k, counts, offsets, sorted_slot, sc,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_prepared_weight_bytes(int E1, int H, int I, int fmt, int which) {
+  if (E1 <= 0 || H <= 0 || I <= 0 || (fmt != MX_E4M3 && fmt != MX_E2M1)) return 0;
+  if (H % 128 || I % 128) return 0;
+  if (which == 1) return prepared_layout(E1, 2 * I, H, fmt).total_bytes;
+  if (which == 2) return prepared_layout(E1, H, I, fmt).total_bytes;
+  return 0;
+}
+
+int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int H, int I, int fmt,
+                        int which, void* dst, size_t dst_bytes, mx_stream_t stream) {
+  if (E1 <= 0 || H <= 0 || I <= 0 || (fmt != MX_E4M3 && fmt != MX_E2M1) || (which != 1 && which != 2))
+    return MX_ERR_INVALID_ARG;
+  if (!codes || !scales || !dst) return MX_ERR_INVALID_ARG;
+  if (H % 128 || I % 128) return MX_ERR_UNSUPPORTED;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(dst, 256)) return MX_ERR_ALIGNMENT;
+  const PreparedLayout L = which == 1 ? prepared_layout(E1, 2 * I, H, fmt) : prepared_layout(E1, H, I, fmt);
+  if (dst_bytes < L.total_bytes) return MX_ERR_WORKSPACE;
+  return cuda_status(launch_prepare_weights(codes, scales, L, static_cast<uint8_t*>(dst),
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_gemm_workspace_size(int T, int H, int I, int E, int k) {
+  if (check_gemm_shape(T, H, I, E, k, MX_E4M3) != MX_OK) return 0;
+  return al256(256) + al256(static_cast<size_t>(T) * (k + 1) * H);
+}
+
+int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
+                            const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
+                            int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
+                            uint8_t* h_scales, void* ws, size_t ws_bytes, mx_stream_t stream) {
+  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  if (st != MX_OK) return st;
+  if (!offsets || !w1_prep || !ws) return MX_ERR_INVALID_ARG;
+  if (T == 0) return MX_OK;
+  if (!act_codes || !act_scales || !sorted_slot || !h_codes || !h_scales) return MX_ERR_INVALID_ARG;
+  if (!aligned(act_codes, 16) || !aligned(act_scales, 16) || !aligned(h_codes, 16) ||
+      !aligned(w1_prep, 256) || !aligned(ws, 256))
+    return MX_ERR_ALIGNMENT;
+  if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  return run_gemm1(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k, h_codes,
+                   h_scales, reinterpret_cast<int*>(w), w + al256(256),
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
+                                  const int32_t* offsets, const int32_t* sorted_slot,
+                                  const float* topk_w, const void* w2_prep, int fmt, int T, int H,
+                                  int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                                  mx_stream_t stream) {
+  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  if (st != MX_OK) return st;
+  if (!offsets || !w2_prep || !ws) return MX_ERR_INVALID_ARG;
+  if (T == 0) return MX_OK;
+  if (!h_codes || !h_scales || !sorted_slot || !topk_w || !out) return MX_ERR_INVALID_ARG;
+  if (!aligned(h_codes, 16) || !aligned(h_scales, 16) || !aligned(out, 16) || !aligned(w2_prep, 256) ||
+      !aligned(ws, 256))
+    return MX_ERR_ALIGNMENT;
+  if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
+  return run_gemm2(h_codes, h_scales, offsets, sorted_slot, topk_w, w2_prep, fmt, T, H, I, E, k, out,
+                   reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt) {
+  if (check_gemm_shape(T, H, I, E, k, fmt) != MX_OK) return 0;
+  return carve_forward(nullptr, T, H, I, E, k).bytes;
+}
+
+int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
+                int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                mx_stream_t stream) {
+  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  if (st != MX_OK) return st;
+  if (T == 0) return MX_OK;
+  if (!x_bf16 || !logits || !w1_prep || !w2_prep || !out || !ws) return MX_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(out, 16) || !aligned(w1_prep, 256) || !aligned(w2_prep, 256) ||
+      !aligned(ws, 256))
+    return MX_ERR_ALIGNMENT;
+  if (ws_bytes < moe_workspace_size(T, H, I, E, k, fmt)) return MX_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const ForwardWs f = carve_forward(ws, T, H, I, E, k);
+  if (launch_zero(out, static_cast<size_t>(T) * H * 4, s) != cudaSuccess) return MX_ERR_CUDA;
+  if (launch_quantize_act(x_bf16, static_cast<int64_t>(T) * H, f.act_codes, f.act_scales, s) != cudaSuccess)
+    return MX_ERR_CUDA;
+  if (launch_topk(logits, T, E, k, f.ids, f.topk_w, s) != cudaSuccess) return MX_ERR_CUDA;
+  if (launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
+    return MX_ERR_CUDA;
+  st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s);
+  if (st != MX_OK) return st;
+  return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
+                   k, out, f.perm.status, s);
+}
+
+int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {
+  if (!ws || !host_status) return MX_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MX_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MX_ERR_CUDA;
+  *host_status = v;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return MX_ERR_CUDA;
+  return MX_OK;
+}
+
+void mx_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+}  // extern "C"

@@ -1,0 +1,607 @@
+// Grouped MX block-scaled GEMMs of the MoE expert layer on tcgen05 tensor
+// cores (sm_103a), one persistent warp-specialised kernel for both:
+//
+//   epi 0 (gate/up):  D_gate = Wg[e] . X^T, D_up = Wu[e] . X^T over K = H, then
+//                     h = silu(D_gate) * D_up re-quantised to MXFP8 per 32 rows
+//                     of I in the epilogue;
+//   epi 1 (down):     D = Wd[e] . h^T over K = I, then out[t] += w * D in the
+//                     epilogue (fp32 atomic adds: the weighted combine).
+//
+// Weights are the MMA's A operand (M = 128 rows per sub-tile, two sub-tiles per
+// tile), the expert's token rows are the B operand (N = the tile's token count
+// rounded up to 16, at most `bn`), so a decode tile with two tokens still runs
+// full-width M = 128 MMAs while streaming weights ("swap-AB").  Tiles are
+// (expert, weight rows, token rows), expert-major, handed out round-robin to
+// one CTA per SM; per-expert token counts are read from the device-side
+// permutation offsets, so nothing waits on the host.
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
+//               unpacked to the 16-byte-aligned form by the TMA), their
+//               512-byte scale blocks (bulk copy), token rows (tensor map)
+//   warp 1      TMEM allocation; one thread issues tcgen05.cp for the weight
+//               scales and tcgen05.mma.kind::mxf8f6f4.block_scale
+//   warps 4-7   token-row scale staging: tcgen05.st of the B scale factors
+//               into every TMEM lane quarter
+//   warps 8-11  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
+//               MXFP8 re-quantisation or weighted combine
+// Every wait is bounded (wall clock); a wait that runs out sets
+// MX_ERR_TIMEOUT in the status word and every role unwinds.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mxk {
+
+constexpr int kThreads = 384;
+constexpr int kWarpTma = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpSf0 = 4;
+constexpr int kWarpEpi0 = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfColsPerStage = 24;  // SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
+constexpr int kMaxStages = 8;
+
+struct GemmParams {
+  int epi, afmt, T, H, I, E, k;
+  int K, NK, NM, RB;
+  int bn, stages, acc_bufs;
+  int n_rows;
+  uint32_t a_tx;
+  const uint8_t* w_scales;
+  const uint8_t* b_scales;
+  const int32_t* offsets;
+  const int32_t* sorted_slot;
+  const float* topk_w;
+  uint8_t* h_codes;
+  uint8_t* h_scales;
+  float* out;
+  int* status;
+  unsigned long long wait_limit_ns;
+  uint32_t off_a, off_b, off_sfa, off_sfbt, off_meta, off_bar;
+  uint32_t sf_col0;
+  int sfbt_stride;  // words per row of the per-tile B scale table (NK + 1)
+};
+
+struct Tile {
+  int e, m, rows, p0;
+};
+
+struct Shared {
+  uint8_t* base;
+  int* offs;     // [E+2]
+  int* prefix;   // [E+2] tile prefix
+  volatile int* abort_flag;
+  uint64_t* full;
+  uint64_t* empty;
+  uint64_t* sfb_ready;
+  uint64_t* acc_full;
+  uint64_t* acc_empty;
+  uint64_t* drain;
+  uint64_t* sfbt_full;   // per-tile B scale table loaded (128 arrivals)
+  uint64_t* sfbt_empty;  // per-tile B scale table consumed (4 arrivals)
+  uint32_t* tmem_slot;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int NM, int bn) {
+  int lo = 0, hi = E;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (sh.prefix[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  Tile tl;
+  tl.e = lo;
+  const int local = t - sh.prefix[lo];
+  const int nt = local / NM;
+  tl.m = local - nt * NM;
+  const int cnt = sh.offs[lo + 1] - sh.offs[lo];
+  const int n0 = nt * bn;
+  tl.rows = min(bn, cnt - n0);
+  tl.p0 = sh.offs[lo] + n0;
+  return tl;
+}
+
+// Wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
+                                         unsigned long long limit_ns, int* status) {
+  const uint32_t b = smem_u32(bar);
+  if (mbar_try_wait(b, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(b, parity)) return true;
+    if (*sh.abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      set_status(status, MX_ERR_TIMEOUT);
+      *sh.abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+// Whole-warp form of wait_bar: every lane polls, and the outcome is made
+// uniform so that the warp leaves (or continues) together.
+__device__ __forceinline__ bool warp_wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
+                                              unsigned long long limit_ns, int* status) {
+  const bool ok = wait_bar(sh, bar, parity, limit_ns, status);
+  return __all_sync(0xffffffffu, ok) != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_b) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = p.stages;
+
+  Shared sh;
+  sh.base = base;
+  sh.offs = reinterpret_cast<int*>(base + p.off_meta);
+  sh.prefix = sh.offs + (p.E + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + p.off_bar);
+  sh.full = bars;
+  sh.empty = bars + S;
+  sh.sfb_ready = bars + 2 * S;
+  sh.acc_full = bars + 3 * S;
+  sh.acc_empty = bars + 3 * S + 2;
+  sh.drain = bars + 3 * S + 4;
+  sh.sfbt_full = bars + 3 * S + 5;
+  sh.sfbt_empty = bars + 3 * S + 6;
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 7);
+  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S + 8);
+
+  // ---- prologue: expert offsets, per-expert tile counts and their prefix
+  const int E1 = p.E + 1;
+  for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = __ldg(&p.offsets[i]);
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&sh.full[s]), 1);
+      mbar_init(smem_u32(&sh.empty[s]), 1);
+      mbar_init(smem_u32(&sh.sfb_ready[s]), 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sh.acc_full[a]), 1);
+      mbar_init(smem_u32(&sh.acc_empty[a]), 4);
+    }
+    mbar_init(smem_u32(sh.drain), 1);
+    mbar_init(smem_u32(sh.sfbt_full), 128);
+    mbar_init(smem_u32(sh.sfbt_empty), 4);
+    *sh.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(sh.tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  // tile prefix: each thread owns a run of experts, warp 0..11 shuffle-scan
+  {
+    __shared__ int warp_tot[kThreads / 32];
+    const int per = (E1 + kThreads - 1) / kThreads;
+    const int b0 = min(tid * per, E1), b1 = min(b0 + per, E1);
+    int run = 0;
+    for (int e = b0; e < b1; ++e) {
+      const int cnt = sh.offs[e + 1] - sh.offs[e];
+      run += p.NM * ((cnt + p.bn - 1) / p.bn);
+    }
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int acc = incl - run;
+    for (int w = 0; w < warp; ++w) acc += warp_tot[w];
+    for (int e = b0; e < b1; ++e) {
+      sh.prefix[e] = acc;
+      const int cnt = sh.offs[e + 1] - sh.offs[e];
+      acc += p.NM * ((cnt + p.bn - 1) / p.bn);
+    }
+    if (b1 == E1 && b0 < b1) sh.prefix[E1] = acc;
+    if (E1 == 0 && tid == 0) sh.prefix[0] = 0;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *sh.tmem_slot;
+  const int total = sh.prefix[E1];
+  const int NK = p.NK;
+
+  if (warp == kWarpTma) {
+    // ================================================================ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_a);
+      prefetch_tensormap(&tm_b);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+        int rb0, rb1;
+        bool two;
+        if (p.epi == 0) {
+          rb0 = tl.m;
+          rb1 = p.RB / 2 + tl.m;
+          two = true;
+        } else {
+          rb0 = 2 * tl.m;
+          rb1 = 2 * tl.m + 1;
+          two = rb1 < p.RB;
+        }
+        const uint32_t bytes = (p.a_tx + 512u) * (two ? 2u : 1u) + static_cast<uint32_t>(p.bn) * 128u;
+        for (int kc = 0; kc < NK; ++kc, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = smem_u32(&sh.full[s]);
+          mbar_arrive_expect_tx(full, bytes);
+          uint8_t* a_s = base + p.off_a + static_cast<uint32_t>(s) * 32768u;
+          uint8_t* sfa_s = base + p.off_sfa + static_cast<uint32_t>(s) * 1024u;
+          const int blk0 = (tl.e * p.RB + rb0) * NK + kc;
+          tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
+          bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, 512u, full);
+          if (two) {
+            const int blk1 = (tl.e * p.RB + rb1) * NK + kc;
+            tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
+            bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
+          }
+          tma_load_2d(smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u), &tm_b,
+                      kc * 128, tl.p0, full);
+        }
+      }
+      // drain: every fill this thread armed has landed before the CTA exits
+      const uint32_t n_fills = it;
+      for (int s = 0; s < S && static_cast<uint32_t>(s) < n_fills; ++s) {
+        const uint32_t last = n_fills - 1 - ((n_fills - 1 - s) % S);
+        mbar_wait(smem_u32(&sh.full[s]), (last / S) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tcount = 0;
+      const uint32_t afmt = p.afmt == MX_E4M3 ? kFmtE4M3 : kFmtE2M1;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+        const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+        const bool two = p.epi == 0 || (2 * tl.m + 1 < p.RB);
+        uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
+        if (n_mma < 16) n_mma = 16;
+        const uint32_t ab = tcount % static_cast<uint32_t>(p.acc_bufs);
+        const uint32_t aph = (tcount / static_cast<uint32_t>(p.acc_bufs)) & 1u;
+        if (!wait_bar(sh, &sh.acc_empty[ab], aph ^ 1u, p.wait_limit_ns, p.status)) break;
+        tc_fence_after();
+        const uint32_t d0 = tbase + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
+        const uint32_t d1 = tbase + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
+        for (int kc = 0; kc < NK; ++kc, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          if (!wait_bar(sh, &sh.full[s], ph, p.wait_limit_ns, p.status) ||
+              !wait_bar(sh, &sh.sfb_ready[s], ph, p.wait_limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf = tbase + p.sf_col0 + static_cast<uint32_t>(s) * kSfColsPerStage;
+          const uint32_t sfa_s = smem_u32(base + p.off_sfa + static_cast<uint32_t>(s) * 1024u);
+          tmem_cp_32x128b_warpx4(sf + 0u, smem_desc(sfa_s, 0, 128, kSwizzleNone));
+          if (two) tmem_cp_32x128b_warpx4(sf + 8u, smem_desc(sfa_s + 512u, 0, 128, kSwizzleNone));
+          const uint32_t a_s = smem_u32(base + p.off_a + static_cast<uint32_t>(s) * 32768u);
+          const uint32_t b_s = smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u);
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb) {
+            const uint32_t idesc = idesc_mx(afmt, kFmtE4M3, 128, n_mma, kb, kb);
+            const uint64_t bd = smem_desc(b_s + kb * 32, 16, 1024, kSwizzle128B);
+            const uint32_t acc = (kc | kb) != 0 ? 1u : 0u;
+            mma_mxf8f6f4(d0, smem_desc(a_s + kb * 32, 16, 1024, kSwizzle128B), bd, idesc, sf + 0u,
+                         sf + 16u, acc);
+            if (two)
+              mma_mxf8f6f4(d1, smem_desc(a_s + 16384u + kb * 32, 16, 1024, kSwizzle128B), bd, idesc,
+                           sf + 8u, sf + 16u, acc);
+          }
+          mma_commit(smem_u32(&sh.empty[s]));
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&sh.acc_full[ab]));
+      }
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(smem_u32(sh.drain));
+      mbar_wait(smem_u32(sh.drain), 0, 100000000ull);
+    }
+  } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
+    // ================================================================ B scale staging
+    const int q = warp & 3;
+    const int sft = tid - kWarpSf0 * 32;
+    uint32_t* sfbt = reinterpret_cast<uint32_t*>(base + p.off_sfbt);
+    const int stride = p.sfbt_stride;
+    const int K32 = p.K / 32;
+    uint32_t it = 0, tj = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tj) {
+      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      // the previous tile's table has been consumed by all four warps
+      if (!warp_wait_bar(sh, sh.sfbt_empty, (tj & 1u) ^ 1u, p.wait_limit_ns, p.status)) break;
+      for (int idx = sft; idx < p.bn * NK; idx += 128) {
+        const int r = idx / NK, c = idx - r * NK;
+        uint32_t v = 0x7F7F7F7Fu;
+        if (r < tl.rows) {
+          int src_row = tl.p0 + r;
+          if (p.epi == 0) {
+            const int slot = __ldg(&p.sorted_slot[tl.p0 + r]);
+            src_row = slot / (p.k + 1);
+            if (src_row < 0 || src_row >= p.T) {
+              set_status(p.status, MX_ERR_DEVICE_ARG);
+              src_row = 0;
+            }
+          }
+          v = __ldg(reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32) + c);
+        }
+        sfbt[r * stride + c] = v;
+      }
+      mbar_arrive(smem_u32(sh.sfbt_full));
+      if (!warp_wait_bar(sh, sh.sfbt_full, tj & 1u, p.wait_limit_ns, p.status)) break;
+      for (int kc = 0; kc < NK; ++kc, ++it) {
+        const int s = static_cast<int>(it % S);
+        const uint32_t ph = (it / S) & 1u;
+        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = 32 * j + lane;
+          w[j] = r < p.bn ? sfbt[r * stride + kc] : 0x7F7F7F7Fu;
+        }
+        const uint32_t col = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 +
+                             static_cast<uint32_t>(s) * kSfColsPerStage + 16u;
+        __syncwarp();
+        tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.sfb_ready[s]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(sh.sfbt_empty));
+    }
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+    // ================================================================ epilogue
+    const int q = warp & 3;
+    uint32_t tcount = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      const uint32_t ab = tcount % static_cast<uint32_t>(p.acc_bufs);
+      const uint32_t aph = (tcount / static_cast<uint32_t>(p.acc_bufs)) & 1u;
+      if (!warp_wait_bar(sh, &sh.acc_full[ab], aph, p.wait_limit_ns, p.status)) break;
+      tc_fence_after();
+      __syncwarp();
+      const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+      const uint32_t d0 = tbase + lane_base + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
+      const uint32_t d1 = tbase + lane_base + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
+      if (p.epi == 0) {
+        const int i = tl.m * 128 + 32 * q + lane;
+        const int I32 = p.I / 32;
+        for (int c0 = 0; c0 < tl.rows; c0 += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld_32x32b_x16(d0 + c0, g);
+          tmem_ld_32x32b_x16(d1 + c0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const int n = c0 + cc;
+            if (n >= tl.rows) break;
+            const float gv = __uint_as_float(g[cc]);
+            const float uv = __uint_as_float(u[cc]);
+            const float h = gv / (1.0f + __expf(-gv)) * uv;
+            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(h) & 0x7FFFFFFFu);
+            const int s = mx_block_exponent(amax, 8);
+            const uint32_t code = enc_e4m3(h * pow2_neg(s));
+            const size_t row = static_cast<size_t>(tl.p0 + n);
+            p.h_codes[row * p.I + i] = static_cast<uint8_t>(code);
+            if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>(s + 127);
+          }
+        }
+      } else {
+        const bool two = 2 * tl.m + 1 < p.RB;
+        for (int c0 = 0; c0 < tl.rows; c0 += 32) {
+          // lane n: token and combine weight of column c0 + n
+          int tok = 0;
+          float wt = 0.0f;
+          if (c0 + lane < tl.rows) {
+            const int slot = __ldg(&p.sorted_slot[tl.p0 + c0 + lane]);
+            const int tt = slot / (p.k + 1), j = slot - tt * (p.k + 1);
+            if (tt >= 0 && tt < p.T) {
+              tok = tt;
+              wt = j == p.k ? 1.0f : __ldg(&p.topk_w[static_cast<size_t>(tt) * p.k + j]);
+            } else {
+              set_status(p.status, MX_ERR_DEVICE_ARG);
+            }
+          }
+          for (int sub = 0; sub < (two ? 2 : 1); ++sub) {
+            const uint32_t d = sub == 0 ? d0 : d1;
+            const int o = tl.m * 256 + sub * 128 + 32 * q + lane;
+            for (int h0 = 0; h0 < 32 && c0 + h0 < tl.rows; h0 += 16) {
+              uint32_t a[16];
+              __syncwarp();
+              tmem_ld_32x32b_x16(d + c0 + h0, a);
+              tmem_ld_wait();
+#pragma unroll
+              for (int cc = 0; cc < 16; ++cc) {
+                const int n = h0 + cc;
+                const int tn = __shfl_sync(0xffffffffu, tok, n);
+                const float wn = __shfl_sync(0xffffffffu, wt, n);
+                if (c0 + n < tl.rows && wn != 0.0f)
+                  atomicAdd(p.out + static_cast<size_t>(tn) * p.H + o, wn * __uint_as_float(a[cc]));
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[ab]));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+static int sm_count_gemm() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 152;
+  }
+  return n;
+}
+
+// Transaction bytes one weight-block TMA adds to its mbarrier: the bytes read
+// from global memory (MXFP4 blocks are 8 KB packed, 16 KB once unpacked into
+// shared memory).
+static uint32_t weight_block_tx_bytes(int fmt) { return fmt == MX_E4M3 ? 16384u : 8192u; }
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  GemmParams p{};
+  p.epi = a.epi;
+  p.afmt = a.fmt;
+  p.T = a.T;
+  p.H = a.H;
+  p.I = a.I;
+  p.E = a.E;
+  p.k = a.k;
+  const int rows = a.epi == 0 ? 2 * a.I : a.H;
+  p.K = a.epi == 0 ? a.H : a.I;
+  p.NK = p.K / 128;
+  p.RB = rows / 128;
+  p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
+  p.bn = a.bn;
+  p.acc_bufs = a.bn <= 64 ? 2 : 1;
+  p.n_rows = a.n_rows;
+  p.a_tx = weight_block_tx_bytes(a.fmt);
+  const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt);
+  p.w_scales = static_cast<const uint8_t*>(a.w_prep) + L.scales_offset;
+  p.b_scales = a.b_scales;
+  p.offsets = a.offsets;
+  p.sorted_slot = a.sorted_slot;
+  p.topk_w = a.topk_w;
+  p.h_codes = a.h_codes;
+  p.h_scales = a.h_scales;
+  p.out = a.out;
+  p.status = a.status;
+  p.wait_limit_ns = a.wait_limit_ns;
+  p.sfbt_stride = p.NK + 1;
+  p.sf_col0 = 2u * static_cast<uint32_t>(p.acc_bufs) * static_cast<uint32_t>(p.bn);
+
+  // shared memory plan
+  const uint32_t sfbt_bytes = (static_cast<uint32_t>(p.bn) * p.sfbt_stride * 4u + 1023u) & ~1023u;
+  const uint32_t meta_bytes = (static_cast<uint32_t>(a.E + 2) * 8u + 127u) & ~127u;
+  const uint32_t per_stage = 32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int max_smem = 0;
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/;
+  int stages = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
+  if (stages > kMaxStages) stages = kMaxStages;
+  const int tmem_room = static_cast<int>((kTmemCols - p.sf_col0) / kSfColsPerStage);
+  if (stages > tmem_room) stages = tmem_room;
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  uint32_t off = 0;
+  p.off_a = off;
+  off += static_cast<uint32_t>(stages) * 32768u;
+  p.off_b = off;
+  off += static_cast<uint32_t>(stages) * p.bn * 128u;
+  p.off_sfa = off;
+  off += static_cast<uint32_t>(stages) * 1024u;
+  p.off_sfbt = off;
+  off += sfbt_bytes;
+  p.off_meta = off;
+  off += meta_bytes;
+  p.off_bar = off;
+  off += 512u;
+  const size_t smem = static_cast<size_t>(off) + 1024u;
+
+  // tensor maps
+  CUtensorMap tm_a, tm_b;
+  const size_t nblk = static_cast<size_t>(a.E + 1) * p.RB * p.NK;
+  {
+    cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(nblk)};
+    cuuint64_t strides[2];
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUtensorMapDataType dt;
+    if (a.fmt == MX_E4M3) {
+      dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+      strides[0] = 128;
+      strides[1] = 16384;
+    } else {
+      dt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+      strides[0] = 64;
+      strides[1] = 8192;
+    }
+    CUresult r = encode(&tm_a, dt, 3, const_cast<void*>(a.w_prep), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(a.n_rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(p.bn)};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.b_codes), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+
+  cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  // upper bound on tiles: NM * sum_e ceil(count_e / bn) <= NM * (E + 1 + rows / bn)
+  const long long bound =
+      static_cast<long long>(p.NM) * (a.E + 1 + (a.n_rows + p.bn - 1) / p.bn);
+  int grid = sm_count_gemm();
+  if (bound < grid) grid = static_cast<int>(bound > 0 ? bound : 1);
+  k_grouped_gemm<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
+  return cudaGetLastError();
+}
+
+}  // namespace mxk

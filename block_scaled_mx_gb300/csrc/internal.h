@@ -1,0 +1,76 @@
+// Internal launcher interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Launchers only enqueue work; argument checks happen in
+// api.cu.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mxk {
+
+// ---- prep.cu
+cudaError_t launch_quantize_act(const void* x, int64_t n_elems, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t s);
+cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, uint8_t* codes,
+                                    uint8_t* scales, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                        cudaStream_t s);
+
+// Scratch of the permutation: status word, chunk histograms, per-slot local
+// ranks, chunk bases and the last-block counter.
+struct PermuteScratch {
+  int* status;
+  int* chunk_counts;   // [nchunks][E]
+  int* chunk_base;     // [nchunks][E]
+  int* local_rank;     // [T*k]
+  unsigned* done;      // 1 counter
+};
+constexpr int kPermuteChunk = 256;
+size_t permute_scratch_bytes(int T, int E, int k);
+PermuteScratch permute_scratch_carve(void* ws, int T, int E, int k);
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* sorted_slot, const PermuteScratch& sc,
+                           cudaStream_t s);
+
+// dst[p, :] = src[sorted_slot[p] / (k+1), :] for p < n_rows (rows of `row_bytes`).
+cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
+                               const int32_t* sorted_slot, int k, int n_rows, uint8_t* dst,
+                               int* status, cudaStream_t s);
+
+// Kernel layout of one weight table (see gemm.cu): codes in 128-row x
+// 128-element blocks, block (e, rb, kc) at ((e*RB + rb)*NK + kc); scales in
+// 512-byte blocks in the tensor-memory order of the block-scaled MMA.
+struct PreparedLayout {
+  int E1, rows, K, fmt;
+  int RB, NK;
+  size_t block_code_bytes;  // 16384 (E4M3) or 8192 (E2M1)
+  size_t codes_bytes, scales_offset, scales_bytes, total_bytes;
+};
+PreparedLayout prepared_layout(int E1, int rows, int K, int fmt);
+cudaError_t launch_prepare_weights(const uint8_t* codes, const uint8_t* scales,
+                                   const PreparedLayout& L, uint8_t* dst, cudaStream_t s);
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
+
+// ---- gemm.cu
+struct GemmArgs {
+  int epi;               // 0: gate/up + SwiGLU + requant, 1: down + combine
+  int fmt;               // weight format (MX_E4M3 / MX_E2M1)
+  int T, H, I, E, k;
+  const void* w_prep;    // prepared weights
+  const uint8_t* b_codes;   // B operand rows [n_rows, K] (sorted order)
+  int n_rows;               // T*(k+1)
+  const uint8_t* b_scales;  // GEMM1: act scales [T, H/32] by token; GEMM2: h scales [rows, I/32]
+  const int32_t* offsets;   // [E+2]
+  const int32_t* sorted_slot;
+  const float* topk_w;      // GEMM2
+  uint8_t* h_codes;         // GEMM1 out
+  uint8_t* h_scales;        // GEMM1 out
+  float* out;               // GEMM2 out
+  int* status;
+  int bn;                   // N tile (32 or 128)
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
+
+}  // namespace mxk

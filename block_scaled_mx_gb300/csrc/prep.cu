@@ -1,0 +1,502 @@
+// Memory-bound kernels of the MX MoE layer: activation / weight MX
+// quantisation, router top-k with softmax, the device-side token -> expert
+// permutation, the activation row gather and the load-time weight re-layout.
+//
+// All of these are HBM- or launch-latency-bound: 128-bit coalesced loads,
+// grid sizes in multiples of the SM count, no tensor cores.
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mxk {
+
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 152;
+  }
+  return n;
+}
+
+static unsigned grid_for(int64_t work_items, int threads, int per_sm) {
+  int64_t blocks = (work_items + threads - 1) / threads;
+  int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<unsigned>(blocks);
+}
+
+// ------------------------------------------------------------------ activation quantisation
+// One thread = 8 bf16 (one 16-byte load); four consecutive lanes = one MX block
+// of 32.  Block amax over the bf16 magnitudes (integer max of the 15-bit
+// magnitude is monotonic), shared exponent from its bits, exact scaling by
+// 2^-s in fp32, then RNE/saturating E4M3 encoding.
+__global__ void __launch_bounds__(256) k_quantize_act(const uint4* __restrict__ x, int64_t n8,
+                                                      uint2* __restrict__ codes,
+                                                      uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - lane < n8;
+       i += stride) {
+    const bool valid = i < n8;
+    const uint4 v = valid ? __ldg(&x[i]) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t amax = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      amax = max(amax, w[m] & 0x7FFFu);
+      amax = max(amax, (w[m] >> 16) & 0x7FFFu);
+    }
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int s = mx_block_exponent(amax << 16, 8);
+    const float p = pow2_neg(s);
+    uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t c0 = enc_e4m3(__uint_as_float(w[m] << 16) * p);
+      const uint32_t c1 = enc_e4m3(__uint_as_float(w[m] & 0xFFFF0000u) * p);
+      packed[m >> 1] |= (c0 | (c1 << 8)) << ((m & 1) * 16);
+    }
+    if (valid) {
+      codes[i] = make_uint2(packed[0], packed[1]);
+      if ((lane & 3) == 0) scales[i >> 2] = static_cast<uint8_t>(s + 127);
+    }
+  }
+}
+
+cudaError_t launch_quantize_act(const void* x, int64_t n_elems, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t s) {
+  const int64_t n8 = n_elems / 8;
+  if (n8 == 0) return cudaSuccess;
+  k_quantize_act<<<grid_for(n8, 256, 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8,
+                                                      reinterpret_cast<uint2*>(codes), scales);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ weight quantisation
+// One thread = 4 fp32 (one 16-byte load); eight consecutive lanes = one block.
+__global__ void __launch_bounds__(256) k_quantize_weights(const float4* __restrict__ w, int64_t n4,
+                                                          int fmt, uint8_t* __restrict__ codes,
+                                                          uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int emax = fmt == MX_E4M3 ? 8 : 2;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - lane < n4;
+       i += stride) {
+    const bool valid = i < n4;
+    const float4 v = valid ? __ldg(&w[i]) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float f[4] = {v.x, v.y, v.z, v.w};
+    uint32_t amax = 0;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) amax = max(amax, __float_as_uint(f[m]) & 0x7FFFFFFFu);
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+    const int s = mx_block_exponent(amax, emax);
+    const float p = pow2_neg(s);
+    if (valid) {
+      if (fmt == MX_E4M3) {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) packed |= enc_e4m3(f[m] * p) << (8 * m);
+        reinterpret_cast<uint32_t*>(codes)[i] = packed;
+      } else {
+        uint32_t packed = 0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) packed |= enc_e2m1(f[m] * p) << (4 * m);
+        reinterpret_cast<uint16_t*>(codes)[i] = static_cast<uint16_t>(packed);
+      }
+      if ((lane & 7) == 0) scales[i >> 3] = static_cast<uint8_t>(s + 127);
+    }
+  }
+}
+
+cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, uint8_t* codes,
+                                    uint8_t* scales, cudaStream_t s) {
+  const int64_t n4 = n_elems / 4;
+  if (n4 == 0) return cudaSuccess;
+  k_quantize_weights<<<grid_for(n4, 256, 8), 256, 0, s>>>(reinterpret_cast<const float4*>(w), n4,
+                                                          fmt, codes, scales);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ router top-k
+// One warp per token.  Lane l holds logits l, l+32, ... in registers; each of
+// the k rounds takes the warp-wide maximum (larger logit, then lower index)
+// among the logits not yet taken.  Lane j keeps round j's winner, so ids come
+// out in descending-logit order; softmax over the k winners in fp32.
+template <int PER>
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
+                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const float* row = logits + static_cast<int64_t>(t) * E;
+  float v[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? __ldg(&row[e]) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float my_v = -INFINITY;
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == INT_MAX)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
+  }
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
+  float ex = lane < k ? expf(my_v - vmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    ids[static_cast<int64_t>(t) * k + lane] = my_i;
+    wout[static_cast<int64_t>(t) * k + lane] = ex / sum;
+  }
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                        cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((T + 7) / 8);
+  if (E <= 32) k_topk<1><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (E <= 128) k_topk<4><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else if (E <= 512) k_topk<16><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  else k_topk<32><<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ permutation
+// Stable counting sort of the T*k routed slots by expert, with the T shared
+// slots appended, without atomics whose order could leak into the result:
+//  pass 1 (one block per chunk of 256 tokens): per warp, a bitmask per expert
+//    of the lanes (tokens) routed to it; a slot's rank inside its chunk is the
+//    popcount of lower lanes plus the popcounts of earlier warps.  The block
+//    writes its per-expert counts; the last block to finish (threadfence +
+//    counter) sums them into counts / offsets and turns them into per-chunk
+//    bases (experts ascending, chunks ascending).
+//  pass 2: each slot lands at chunk_base + rank.
+// With a single chunk, pass 1 finishes the scatter itself.
+size_t permute_scratch_bytes(int T, int E, int k) {
+  const size_t nchunks = static_cast<size_t>((T + kPermuteChunk - 1) / kPermuteChunk);
+  auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  return al(256) + al(nchunks * E * 4) * 2 + al(static_cast<size_t>(T) * k * 4) + al(256);
+}
+
+PermuteScratch permute_scratch_carve(void* ws, int T, int E, int k) {
+  const size_t nchunks = static_cast<size_t>((T + kPermuteChunk - 1) / kPermuteChunk);
+  auto al = [](size_t b) { return (b + 255) & ~static_cast<size_t>(255); };
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  PermuteScratch sc;
+  sc.status = reinterpret_cast<int*>(p);
+  p += al(256);
+  sc.chunk_counts = reinterpret_cast<int*>(p);
+  p += al(nchunks * E * 4);
+  sc.chunk_base = reinterpret_cast<int*>(p);
+  p += al(nchunks * E * 4);
+  sc.local_rank = reinterpret_cast<int*>(p);
+  p += al(static_cast<size_t>(T) * k * 4);
+  sc.done = reinterpret_cast<unsigned*>(p);
+  return sc;
+}
+
+__global__ void __launch_bounds__(kPermuteChunk) k_permute_count(
+    const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot, PermuteScratch sc,
+    int nchunks) {
+  extern __shared__ uint32_t bits[];  // [8 warps][E] lane masks, then E+2 ints of scan scratch
+  constexpr int kWarps = kPermuteChunk / 32;
+  __shared__ int s_is_last;
+  __shared__ int s_warp_tot[kWarps];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x;
+  for (int i = tid; i < kWarps * E; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  const int t = chunk * kPermuteChunk + tid;
+  const bool valid = t < T;
+  int my_e[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    my_e[j] = -1;
+    if (j < k && valid) {
+      int e = ids[static_cast<int64_t>(t) * k + j];
+      if (e < 0 || e >= E) {
+        set_status(sc.status, MX_ERR_DEVICE_ARG);
+        e = -1;
+      }
+      my_e[j] = e;
+      if (e >= 0) atomicOr(&bits[warp * E + e], 1u << lane);
+    }
+  }
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  int my_r[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    my_r[j] = 0;
+    if (j < k && my_e[j] >= 0) {
+      const int e = my_e[j];
+      int r = __popc(bits[warp * E + e] & lt);
+      for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
+      my_r[j] = r;
+    }
+  }
+  for (int e = tid; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < kWarps; ++w) c += __popc(bits[w * E + e]);
+    sc.chunk_counts[static_cast<int64_t>(chunk) * E + e] = c;
+  }
+  if (nchunks > 1) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < k && valid) sc.local_rank[static_cast<int64_t>(t) * k + j] = my_r[j];
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_is_last = (atomicAdd(sc.done, 1u) == static_cast<unsigned>(nchunks - 1));
+    __syncthreads();
+    if (!s_is_last) return;
+    __threadfence();
+  } else {
+    __syncthreads();
+  }
+  // ---- last (or only) block: totals, exclusive scan over E+1 experts, chunk bases
+  int* scan = reinterpret_cast<int*>(bits + kWarps * E);  // E+2 ints
+  for (int e = tid; e <= E; e += blockDim.x) {
+    int c = 0;
+    if (e < E) {
+      for (int ch = 0; ch < nchunks; ++ch) c += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
+    } else {
+      c = T;
+    }
+    scan[e] = c;
+    counts[e] = c;
+  }
+  __syncthreads();
+  // block-wide exclusive scan of scan[0..E] (E+1 <= 1025 values): each thread
+  // owns a contiguous run, warp shuffles scan the run totals.
+  const int n = E + 1;
+  const int per = (n + blockDim.x - 1) / blockDim.x;
+  const int b0 = min(tid * per, n), b1 = min(b0 + per, n);
+  int run = 0;
+  for (int i = b0; i < b1; ++i) run += scan[i];
+  int incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) s_warp_tot[warp] = incl;
+  __syncthreads();
+  int warp_base = 0;
+  for (int w = 0; w < warp; ++w) warp_base += s_warp_tot[w];
+  int acc = warp_base + incl - run;
+  __syncthreads();
+  for (int i = b0; i < b1; ++i) {
+    const int c = scan[i];
+    scan[i] = acc;
+    acc += c;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) offsets[e] = scan[e];
+  if (tid == 0) offsets[E + 1] = T * (k + 1);
+  if (nchunks > 1) {
+    for (int e = tid; e < E; e += blockDim.x) {
+      int base = scan[e];
+      for (int ch = 0; ch < nchunks; ++ch) {
+        sc.chunk_base[static_cast<int64_t>(ch) * E + e] = base;
+        base += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
+      }
+    }
+  } else {
+    // single chunk: scatter directly (this block holds every token)
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < k && valid && my_e[j] >= 0)
+        sorted_slot[scan[my_e[j]] + my_r[j]] = t * (k + 1) + j;
+    if (valid) sorted_slot[scan[E] + t] = t * (k + 1) + k;
+  }
+}
+
+__global__ void __launch_bounds__(kPermuteChunk) k_permute_scatter(
+    const int32_t* __restrict__ ids, int T, int E, int k, const int32_t* __restrict__ offsets,
+    int32_t* __restrict__ sorted_slot, PermuteScratch sc) {
+  const int chunk = blockIdx.x;
+  const int t = chunk * kPermuteChunk + threadIdx.x;
+  if (blockIdx.x == 0 && threadIdx.x == 0) *sc.done = 0u;  // ready for the next call
+  if (t >= T) return;
+  for (int j = 0; j < k; ++j) {
+    const int e = ids[static_cast<int64_t>(t) * k + j];
+    if (e < 0 || e >= E) continue;
+    const int pos = sc.chunk_base[static_cast<int64_t>(chunk) * E + e] +
+                    sc.local_rank[static_cast<int64_t>(t) * k + j];
+    sorted_slot[pos] = t * (k + 1) + j;
+  }
+  sorted_slot[offsets[E] + t] = t * (k + 1) + k;
+}
+
+cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* sorted_slot, const PermuteScratch& sc,
+                           cudaStream_t s) {
+  const int nchunks = T == 0 ? 1 : (T + kPermuteChunk - 1) / kPermuteChunk;
+  const size_t smem = static_cast<size_t>(kPermuteChunk / 32) * E * 4 + static_cast<size_t>(E + 2) * 4;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_permute_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+  }
+  k_permute_count<<<nchunks, kPermuteChunk, smem, s>>>(ids, T, E, k, counts, offsets, sorted_slot, sc,
+                                                       nchunks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || nchunks == 1) return e;
+  k_permute_scatter<<<nchunks, kPermuteChunk, 0, s>>>(ids, T, E, k, offsets, sorted_slot, sc);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ row gather
+__global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ src, int T,
+                                                     int64_t row_chunks,
+                                                     const int32_t* __restrict__ sorted_slot, int k,
+                                                     int64_t total_chunks, uint4* __restrict__ dst,
+                                                     int* status) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks;
+       i += stride) {
+    const int64_t p = i / row_chunks, c = i - p * row_chunks;
+    const int t = __ldg(&sorted_slot[p]) / (k + 1);
+    if (t < 0 || t >= T) {
+      set_status(status, MX_ERR_DEVICE_ARG);
+      continue;
+    }
+    dst[i] = __ldg(&src[static_cast<int64_t>(t) * row_chunks + c]);
+  }
+}
+
+cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
+                               const int32_t* sorted_slot, int k, int n_rows, uint8_t* dst,
+                               int* status, cudaStream_t s) {
+  const int64_t row_chunks = row_bytes / 16;
+  const int64_t total = row_chunks * n_rows;
+  if (total == 0) return cudaSuccess;
+  k_gather_rows<<<grid_for(total, 256, 8), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), T,
+                                                        row_chunks, sorted_slot, k, total,
+                                                        reinterpret_cast<uint4*>(dst), status);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ weight re-layout
+PreparedLayout prepared_layout(int E1, int rows, int K, int fmt) {
+  PreparedLayout L;
+  L.E1 = E1;
+  L.rows = rows;
+  L.K = K;
+  L.fmt = fmt;
+  L.RB = rows / 128;
+  L.NK = K / 128;
+  L.block_code_bytes = fmt == MX_E4M3 ? 16384 : 8192;
+  const size_t nblk = static_cast<size_t>(E1) * L.RB * L.NK;
+  L.codes_bytes = nblk * L.block_code_bytes;
+  L.scales_offset = (L.codes_bytes + 1023) & ~static_cast<size_t>(1023);
+  L.scales_bytes = nblk * 512;
+  L.total_bytes = L.scales_offset + L.scales_bytes;
+  return L;
+}
+
+// codes: one thread per 16-byte chunk of the destination block
+__global__ void __launch_bounds__(256) k_prepare_codes(const uint4* __restrict__ src, int rows,
+                                                       int64_t src_row_chunks, int RB, int NK,
+                                                       int blk_row_chunks, int64_t total,
+                                                       uint4* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t per_blk = static_cast<int64_t>(128) * blk_row_chunks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t b = i / per_blk;
+    const int within = static_cast<int>(i - b * per_blk);
+    const int r = within / blk_row_chunks, c = within - r * blk_row_chunks;
+    const int kc = static_cast<int>(b % NK);
+    const int64_t erb = b / NK;
+    const int rb = static_cast<int>(erb % RB);
+    const int64_t e = erb / RB;
+    const int64_t src_row = e * rows + static_cast<int64_t>(rb) * 128 + r;
+    dst[i] = __ldg(&src[src_row * src_row_chunks + static_cast<int64_t>(kc) * blk_row_chunks + c]);
+  }
+}
+
+// scales: one thread per 32-bit word of a 512-byte block: lane l, word j holds
+// the four k-blocks of row 32*j + l (the tensor-memory scale-factor layout of
+// the block-scaled MMA, copied in by tcgen05.cp 32x128b.warpx4).
+__global__ void __launch_bounds__(256) k_prepare_scales(const uint8_t* __restrict__ src, int rows,
+                                                        int K32, int RB, int NK, int64_t total_words,
+                                                        uint32_t* __restrict__ dst) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_words;
+       i += stride) {
+    const int64_t b = i / 128;
+    const int w = static_cast<int>(i & 127);
+    const int l = w >> 2, j = w & 3;
+    const int kc = static_cast<int>(b % NK);
+    const int64_t erb = b / NK;
+    const int rb = static_cast<int>(erb % RB);
+    const int64_t e = erb / RB;
+    const int64_t row = e * rows + static_cast<int64_t>(rb) * 128 + 32 * j + l;
+    dst[i] = __ldg(reinterpret_cast<const uint32_t*>(src + row * K32 + static_cast<int64_t>(kc) * 4));
+  }
+}
+
+cudaError_t launch_prepare_weights(const uint8_t* codes, const uint8_t* scales,
+                                   const PreparedLayout& L, uint8_t* dst, cudaStream_t s) {
+  const int64_t nblk = static_cast<int64_t>(L.E1) * L.RB * L.NK;
+  const int blk_row_chunks = L.fmt == MX_E4M3 ? 8 : 4;
+  const int64_t src_row_chunks = (L.fmt == MX_E4M3 ? L.K : L.K / 2) / 16;
+  const int64_t total = nblk * 128 * blk_row_chunks;
+  if (total > 0) {
+    k_prepare_codes<<<grid_for(total, 256, 8), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(codes), L.rows, src_row_chunks, L.RB, L.NK, blk_row_chunks,
+        total, reinterpret_cast<uint4*>(dst));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t words = nblk * 128;
+    k_prepare_scales<<<grid_for(words, 256, 8), 256, 0, s>>>(
+        scales, L.rows, L.K / 32, L.RB, L.NK, words,
+        reinterpret_cast<uint32_t*>(dst + L.scales_offset));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s) {
+  return cudaMemsetAsync(p, 0, bytes, s);
+}
+
+}  // namespace mxk

@@ -1,0 +1,191 @@
+/*
+ * mxmoe.h -- C ABI of libmxmoe.so, the GB300 (sm_103a) MX block-scaled
+ * sparse-MoE expert layer.
+ *
+ * The layer (one MoE block of a transformer) computes, for T tokens of hidden
+ * size H, E routed experts with intermediate size I and top-k routing, plus one
+ * shared expert folded into the expert table at index E as an always-selected
+ * expert of weight 1:
+ *
+ *   act      = MXFP8(x)                                   mx_quantize_act
+ *   ids, w   = top-k(logits), softmax over the k chosen    moe_route_topk
+ *   slots    = tokens grouped by expert                   moe_permute
+ *   h[s]     = MXFP8( silu(act[t].Wg[e]) * (act[t].Wu[e]) ) moe_grouped_gemm_swiglu
+ *   out[t]  += w[s] * (h[s] . Wd[e])                      moe_grouped_gemm_down_combine
+ *
+ * Sources: the MX weight formats and the shared-expert folding follow
+ * "Tracing the bottleneck: optimising MiniMax M3 on AMD Instinct MI355X"
+ * (opening results list for MXFP8/MXFP4 weights; Figure 4 for the shared
+ * expert placed in the routed table and selected for every token; Figure 3 and
+ * the surrounding passage for separate small-M / large-M schedules; the
+ * passage after Figure 4 for moving weight/scale re-layout to load time).  The
+ * combine fused into the down projection's epilogue follows "Kimi K3
+ * performance in vLLM: 2.8x throughput" (section on fusing the MXFP4 top-k
+ * finalize into the epilogue).  The element formats are those of the OCP
+ * Microscaling Formats (MX) v1.0 specification.
+ *
+ * Conventions for every call
+ *  - Pointers are DEVICE pointers owned by the caller unless stated; the
+ *    library never allocates and never synchronises the stream.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous: they validate arguments on the host, enqueue kernels and
+ *    return.  A return of MX_OK means the work was enqueued.
+ *  - Device-side errors (a bounded wait that ran out, an expert id out of
+ *    range) are OR-ed into a status word at the start of the caller's
+ *    workspace; read and clear it with moe_get_status.
+ *  - Workspaces must be zero-filled once before their first use (the library
+ *    leaves them ready for the next call).
+ *  - Formats: MX_E4M3 (MXFP8, one byte per element) and MX_E2M1 (MXFP4, two
+ *    elements per byte, element 2i in the low nibble).  Every 32 consecutive
+ *    elements along K share one E8M0 scale byte (value 2^(code-127)).
+ *  - Non-finite inputs are a precondition violation: results are unspecified.
+ */
+#ifndef MXMOE_H_
+#define MXMOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* mx_stream_t; /* same type as cudaStream_t */
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+/* ---- status codes ---- */
+#define MX_OK 0
+#define MX_ERR_INVALID_ARG 1  /* null pointer, non-positive size, k > E, k > 32 ... */
+#define MX_ERR_UNSUPPORTED 2  /* shape the kernels do not handle (see each call) */
+#define MX_ERR_ALIGNMENT 3    /* a pointer is not 16-byte (weights: 256-byte) aligned */
+#define MX_ERR_WORKSPACE 4    /* workspace / destination smaller than required */
+#define MX_ERR_CUDA 5         /* a CUDA runtime/driver call or kernel launch failed */
+#define MX_ERR_TIMEOUT 6      /* device status: a bounded wait inside a kernel ran out */
+#define MX_ERR_DEVICE_ARG 7   /* device status: an expert id or slot id out of range */
+
+/* ---- element formats ---- */
+#define MX_E4M3 0
+#define MX_E2M1 1
+
+/* Human-readable name of a status code (static string, never NULL). */
+MX_API const char* mx_status_string(int status);
+
+/* Activation quantisation, bf16 -> MXFP8 (E4M3 codes + E8M0 scales).
+ *   x_bf16  [T, H] row-major bf16.  codes [T, H] bytes.  scales [T, H/32] bytes.
+ * Per row and per block of 32 along H: shared exponent
+ * s = clamp(floor(log2(amax)) - 8, -127, 127) (an all-zero block gives -127),
+ * scale byte s + 127, element code = E4M3 value of x / 2^s rounded to nearest
+ * even and saturated to +-448; a negative value that rounds to zero keeps its
+ * sign (0x80).  Bit-exact with the reference definition.
+ * Errors: MX_ERR_INVALID_ARG (null, T < 0, H <= 0), MX_ERR_UNSUPPORTED
+ * (H % 32), MX_ERR_ALIGNMENT (x or codes not 16-byte aligned). */
+MX_API int mx_quantize_act(const void* x_bf16, int T, int H, uint8_t* codes, uint8_t* scales,
+                    mx_stream_t stream);
+
+/* Weight quantisation, fp32 -> MXFP8 or MXFP4 (load-time helper; same rule as
+ * mx_quantize_act with emax 8 for E4M3 and 2 for E2M1, saturation at 6 for
+ * E2M1).  w [rows, K] fp32; codes [rows, K] (E4M3) or [rows, K/2] (E2M1);
+ * scales [rows, K/32].  Errors as mx_quantize_act (K % 32). */
+MX_API int mx_quantize_weights(const float* w, int64_t rows, int K, int fmt, uint8_t* codes,
+                        uint8_t* scales, mx_stream_t stream);
+
+/* Router: per token, the k largest of E fp32 logits, ties to the lowest expert
+ * index, in descending logit order, and their softmax (over the k selected).
+ *   logits [T, E] fp32; topk_ids [T, k] int32; topk_w [T, k] fp32.
+ * Ids are bit-exact with the reference; weights are fp32 (a few ulp).
+ * Errors: MX_ERR_INVALID_ARG (null, T < 0, E <= 0, k < 1, k > E, k > 32),
+ * MX_ERR_UNSUPPORTED (E > 1024). */
+MX_API int moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                   mx_stream_t stream);
+
+/* Bytes of workspace moe_permute needs. */
+MX_API size_t moe_permute_workspace_size(int T, int E, int k);
+
+/* Token -> expert permutation with the shared expert folded in.
+ *   counts [E+1]: tokens per expert, counts[E] = T (shared expert).
+ *   offsets [E+2]: exclusive prefix of counts, offsets[E+1] = T*(k+1).
+ *   sorted_slot [T*(k+1)]: slot ids t*(k+1)+j (j = k is the shared slot),
+ *     grouped by expert ascending (shared last), tokens ascending inside each
+ *     expert.  Bit-exact, deterministic, no host synchronisation.
+ * topk_ids must hold k distinct ids in [0, E) per token; an id out of range
+ * sets MX_ERR_DEVICE_ARG in the workspace status and is skipped.
+ * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (E > 1024),
+ * MX_ERR_WORKSPACE (ws_bytes < moe_permute_workspace_size). */
+MX_API int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
+                int32_t* sorted_slot, void* ws, size_t ws_bytes, mx_stream_t stream);
+
+/* Bytes of a prepared (kernel-layout) weight table.  which = 1: W1, the
+ * gate/up projection [E1][2I][H] (rows 0..I-1 gate, I..2I-1 up); which = 2:
+ * W2, the down projection [E1][H][I].  E1 = E + 1 experts (shared last). */
+MX_API size_t moe_prepared_weight_bytes(int E1, int H, int I, int fmt, int which);
+
+/* Load-time re-layout of a canonical MX weight table into the kernel layout
+ * (done once per weight set, off the serving path).
+ *   codes  [E1][rows][K] (E4M3) or [E1][rows][K/2] (E2M1), scales [E1][rows][K/32],
+ *   rows/K = 2I/H for which = 1 and H/I for which = 2.
+ *   dst: moe_prepared_weight_bytes(...) bytes, 256-byte aligned.
+ * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H or I not a multiple of
+ * 128), MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE (dst_bytes too small). */
+MX_API int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int H, int I, int fmt,
+                        int which, void* dst, size_t dst_bytes, mx_stream_t stream);
+
+/* Bytes of workspace the two grouped GEMM calls need. */
+MX_API size_t moe_gemm_workspace_size(int T, int H, int I, int E, int k);
+
+/* Grouped gate/up GEMM with SwiGLU and MXFP8 re-quantisation of h fused into
+ * the epilogue.  For every slot position p (expert e = the segment of
+ * `offsets` holding p, token t = sorted_slot[p] / (k+1)):
+ *   g_i = sum_h act[t,h] Wg[e,i,h],  u_i = sum_h act[t,h] Wu[e,i,h]  (fp32 accumulation
+ *   of exactly decoded MX products), h_i = silu(g_i) * u_i, then h quantised
+ *   per 32 along I exactly as mx_quantize_act does.
+ *   act_codes/act_scales: MXFP8 activations [T, H], [T, H/32].
+ *   offsets/sorted_slot: moe_permute output.  w1_prep: moe_prepare_weights(which=1).
+ *   h_codes [T*(k+1), I], h_scales [T*(k+1), I/32]: row p = slot position p.
+ * fp32 accumulation means an h code next to a rounding boundary may differ by
+ * one step from an exact-arithmetic reference.
+ * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H or I % 128, E > 1024),
+ * MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE, MX_ERR_CUDA. */
+MX_API int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
+                            const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
+                            int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
+                            uint8_t* h_scales, void* ws, size_t ws_bytes, mx_stream_t stream);
+
+/* Grouped down GEMM with the weighted scatter-combine fused into the epilogue:
+ *   out[t, :] += w_s * sum_i h[p,i] Wd[e,:,i]   (w_s = topk_w[t,j] for a routed
+ *   slot, 1 for the shared slot), fp32 atomic adds into `out`.
+ *   out [T, H] fp32 must be zero-filled (or hold a residual) by the caller.
+ * Errors: as moe_grouped_gemm_swiglu. */
+MX_API int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
+                                  const int32_t* offsets, const int32_t* sorted_slot,
+                                  const float* topk_w, const void* w2_prep, int fmt, int T, int H,
+                                  int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                                  mx_stream_t stream);
+
+/* Bytes of workspace moe_forward needs (intermediates + GEMM scratch). */
+MX_API size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt);
+
+/* The whole layer in one call, no host synchronisation: quantise, route,
+ * permute, both grouped GEMMs; out [T, H] fp32 is overwritten.
+ * Errors: union of the step calls. */
+MX_API int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
+                int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                mx_stream_t stream);
+
+/* Copy the workspace status word to *host_status (synchronising `stream`) and
+ * clear it.  0 = no device-side error; otherwise an MX_ERR_* code. */
+MX_API int moe_get_status(void* ws, mx_stream_t stream, int* host_status);
+
+/* Test hook: the wall-clock limit, in nanoseconds, of every bounded wait inside
+ * the GEMM kernels (default 2e9).  A tiny limit makes the waits run out, which
+ * exercises the MX_ERR_TIMEOUT path without hanging the GPU. */
+MX_API void mx_debug_set_wait_limit_ns(uint64_t ns);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MXMOE_H_ */

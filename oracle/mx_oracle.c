@@ -190,16 +190,30 @@ int orc_quantize_bf16(const uint16_t* x, int64_t rows, int64_t K, uint8_t* codes
 /* Weight quantisation: fp32 [rows, K] -> MXFP8 or MXFP4. */
 int orc_quantize_f32(const float* w, int64_t rows, int64_t K, int fmt, uint8_t* codes,
                      uint8_t* scales) {
-  if (!w || rows < 0 || K <= 0 || K % 32) return ORC_ERR_ARG;
-  double* row = (double*)malloc(sizeof(double) * (size_t)K);
-  if (!row) return ORC_ERR_NOMEM;
+  if (!w || !codes || !scales || rows < 0 || K <= 0 || K % 32) return ORC_ERR_ARG;
+  if (fmt != ORC_E4M3 && fmt != ORC_E2M1) return ORC_ERR_ARG;
   int64_t row_bytes = (fmt == ORC_E4M3) ? K : K / 2;
   int st = ORC_OK;
-  for (int64_t r = 0; r < rows && st == ORC_OK; ++r) {
-    for (int64_t i = 0; i < K; ++i) row[i] = (double)w[r * K + i];
-    st = orc_quantize_rows(row, 1, K, fmt, codes + r * row_bytes, scales + r * (K / 32));
+  /* rows are independent: one row per iteration */
+#pragma omp parallel
+  {
+    double* rowbuf = (double*)malloc(sizeof(double) * (size_t)K);
+#pragma omp for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+      if (!rowbuf) continue;
+      for (int64_t i = 0; i < K; ++i) rowbuf[i] = (double)w[r * K + i];
+      int rs = orc_quantize_rows(rowbuf, 1, K, fmt, codes + r * row_bytes, scales + r * (K / 32));
+      if (rs) {
+#pragma omp atomic write
+        st = rs;
+      }
+    }
+    if (!rowbuf) {
+#pragma omp atomic write
+      st = ORC_ERR_NOMEM;
+    }
+    free(rowbuf);
   }
-  free(row);
   return st;
 }
 
@@ -269,6 +283,7 @@ static double silu(double z) { return z / (1.0 + exp(-z)); }
 /* Decode an MX matrix [rows, K] (codes in `fmt`, E8M0 scales per 32) to fp64. */
 static void decode_matrix(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K,
                           int fmt, double* out) {
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < K; ++c) {
       double s = orc_decode_e8m0(scales[r * (K / 32) + c / 32]);

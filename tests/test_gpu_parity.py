@@ -1,0 +1,255 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Bit-exact: activation codes/scales, weight codes/scales (both formats), top-k
+ids, counts, offsets, sorted slots.  Tolerances: top-k weights (fp32 softmax
+vs fp64), h codes (fp32 tensor-core accumulation can move a value across a
+rounding boundary: mismatch fraction reported and bounded), and the layer
+output: relative L2 <= 5e-3 and max-abs <= 3% of the output RMS."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_scaled_mx_gb300 import mxmoe as mx
+from block_scaled_mx_gb300 import workload as W
+
+from layer_inputs import OUT_MAX_ABS_OVER_RMS, OUT_REL_L2, build_layer, oracle_forward, out_errors
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as g
+
+    g.build()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+
+
+def _bf16(T, H, seed, scale_rows=True):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T, H, generator=g)
+    if scale_rows:
+        x = x * torch.exp(torch.randn(T, 1, generator=g) * 3)
+    return x.to(torch.bfloat16)
+
+
+# ------------------------------------------------------------------ quantisers
+@pytest.mark.parametrize("T,H", [(1, 32), (16, 256), (37, 4096), (6, 2048), (8192, 4096)])
+def test_quantize_act_bitexact(T, H):
+    x = _bf16(T, H, T * 7 + H)
+    if T > 2:
+        x[0, :32] = 0.0
+        x[1, 3] = -1e-30          # negative that rounds to -0
+        x[2, :32] = 1.0e-39       # all-subnormal bf16 block
+        x[2, 40] = 3.0e38         # near the bf16 maximum
+    xd = x.cuda()
+    codes = torch.empty(T, H, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
+    mx.mx_quantize_act(xd, codes, scales)
+    rc, rs = oracle.quantize_bf16(W.bf16_bits(x))
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    got = codes.cpu().numpy()
+    assert np.array_equal(got, rc), f"{np.count_nonzero(got != rc)} code mismatches"
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("rows,K,std", [(3, 32, 1.0), (256, 4096, 0.02), (129, 1536, 0.02), (64, 128, 1e-20)])
+def test_quantize_weights_bitexact(fmt, rows, K, std):
+    g = torch.Generator().manual_seed(rows + K)
+    w = torch.randn(rows, K, generator=g) * std
+    w[0, :32] = 0.0
+    w[0, 5] = -1e-12      # a negative that rounds to -0 inside a zero-amax-dominated block
+    if K > 32:
+        w[0, 40] = -1e-12
+    if rows > 2:
+        w[1, :32] *= 1e-30   # tiny block
+        w[2, 5] = 7.9        # E2M1 saturation region
+    f = mx.FORMATS[fmt]
+    cdiv = 1 if f == mx.MX_E4M3 else 2
+    codes = torch.empty(rows, K // cdiv, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(rows, K // 32, dtype=torch.uint8, device="cuda")
+    mx.mx_quantize_weights(w.cuda(), f, codes, scales)
+    rc, rs = oracle.quantize_f32(w.numpy(), f)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    got = codes.cpu().numpy()
+    assert np.array_equal(got, rc), f"{np.count_nonzero(got != rc)} code mismatches"
+
+
+# ------------------------------------------------------------------ router, permutation
+@pytest.mark.parametrize("T,E,k,ties", [(16, 8, 2, False), (32, 128, 8, False), (6, 512, 8, False),
+                                        (100, 64, 4, True), (3, 8, 8, True), (8192, 128, 8, False),
+                                        (5, 1000, 32, False)])
+def test_topk(T, E, k, ties):
+    g = torch.Generator().manual_seed(T + E)
+    if ties:
+        logits = torch.randint(-2, 3, (T, E), generator=g).float()
+    else:
+        logits = torch.randn(T, E, generator=g)
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    mx.moe_route_topk(logits.cuda(), k, ids, w)
+    rid, rw = oracle.route_topk(logits.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (16, 8, 2), (32, 128, 8), (6, 512, 8), (300, 16, 4),
+                                   (8192, 128, 8), (513, 1024, 3)])
+def test_permute_bitexact(T, E, k):
+    g = torch.Generator().manual_seed(T * 3 + E)
+    logits = torch.randn(T, E, generator=g)
+    if T >= 300:
+        logits[:, 0] += 3.0   # a skewed expert
+    rid, _ = oracle.route_topk(logits.numpy(), k)
+    ids = torch.from_numpy(rid).cuda()
+    counts = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 2, dtype=torch.int32, device="cuda")
+    ss = torch.empty(T * (k + 1), dtype=torch.int32, device="cuda")
+    ws = mx.alloc_workspace(mx.moe_permute_workspace_size(T, E, k))
+    for _ in range(2):   # second call checks the workspace is left ready
+        ss.fill_(-1)
+        mx.moe_permute(ids, E, counts, offsets, ss, ws)
+        rc, ro, rs = oracle.permute(rid, E)
+        assert np.array_equal(counts.cpu().numpy(), rc)
+        assert np.array_equal(offsets.cpu().numpy(), ro)
+        assert np.array_equal(ss.cpu().numpy(), rs)
+    assert mx.moe_get_status(ws) == 0
+
+
+# ------------------------------------------------------------------ layer
+def _steps(L):
+    wl = L.wl
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    d = "cuda"
+    r = {}
+    r["act_c"] = torch.empty(T, H, dtype=torch.uint8, device=d)
+    r["act_s"] = torch.empty(T, H // 32, dtype=torch.uint8, device=d)
+    mx.mx_quantize_act(L.x, r["act_c"], r["act_s"])
+    r["ids"] = torch.empty(T, k, dtype=torch.int32, device=d)
+    r["w"] = torch.empty(T, k, dtype=torch.float32, device=d)
+    mx.moe_route_topk(L.logits, k, r["ids"], r["w"])
+    r["counts"] = torch.empty(E + 1, dtype=torch.int32, device=d)
+    r["offsets"] = torch.empty(E + 2, dtype=torch.int32, device=d)
+    r["ss"] = torch.empty(T * (k + 1), dtype=torch.int32, device=d)
+    pws = mx.alloc_workspace(mx.moe_permute_workspace_size(T, E, k))
+    mx.moe_permute(r["ids"], E, r["counts"], r["offsets"], r["ss"], pws)
+    gws = mx.alloc_workspace(mx.moe_gemm_workspace_size(T, H, I, E, k))
+    r["h_c"] = torch.empty(T * (k + 1), I, dtype=torch.uint8, device=d)
+    r["h_s"] = torch.empty(T * (k + 1), I // 32, dtype=torch.uint8, device=d)
+    mx.moe_grouped_gemm_swiglu(r["act_c"], r["act_s"], r["offsets"], r["ss"], L.layer.w1, L.fmt, T, H, I, E, k,
+                               r["h_c"], r["h_s"], gws)
+    r["out"] = torch.zeros(T, H, dtype=torch.float32, device=d)
+    mx.moe_grouped_gemm_down_combine(r["h_c"], r["h_s"], r["offsets"], r["ss"], r["w"], L.layer.w2, L.fmt, T, H,
+                                     I, E, k, r["out"], gws)
+    r["status"] = (mx.moe_get_status(pws), mx.moe_get_status(gws))
+    return r
+
+
+def _check_h(r, ref, I):
+    """h codes: GPU rows are slot positions, oracle rows are slot ids."""
+    ss = r["ss"].cpu().numpy()
+    gc = r["h_c"].cpu().numpy()
+    gs = r["h_s"].cpu().numpy()
+    rc = ref["h_codes"][ss]
+    rs = ref["h_scales"][ss]
+    gv = oracle.decode_matrix(gc, gs, oracle.E4M3)
+    rv = oracle.decode_matrix(rc, rs, oracle.E4M3)
+    frac = np.count_nonzero(gc != rc) / gc.size
+    rel = np.linalg.norm(gv - rv) / np.linalg.norm(rv)
+    return frac, rel
+
+
+LAYER_CASES = {
+    "tiny": W.WORKLOADS["tiny"],
+    "decode_mxfp8": W.WORKLOADS["decode_mxfp8"],
+    "decode_mxfp4": W.WORKLOADS["decode_mxfp4"],
+    "specverify_mxfp4": W.WORKLOADS["specverify_mxfp4"],
+    # ragged shapes: two permutation chunks, H = 3*128 (half last down tile)
+    "ragged_e4m3": W.custom("ragged_e4m3", T=300, H=384, I=256, E=16, k=4, fmt="e4m3"),
+    "ragged_e2m1": W.custom("ragged_e2m1", T=77, H=640, I=384, E=12, k=3, fmt="e2m1"),
+    # wide (prefill) schedule with several ragged token tiles per expert
+    "wide_e4m3": W.custom("wide_e4m3", T=1024, H=512, I=256, E=8, k=2, fmt="e4m3", zipf_bias=True),
+    "wide_e2m1": W.custom("wide_e2m1", T=700, H=256, I=384, E=4, k=1, fmt="e2m1"),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
+def test_layer_parity(name):
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    # weights: GPU quantiser vs oracle quantiser, bit-exact
+    for e in range(wl.E + 1):
+        assert np.array_equal(L.w1c[e].cpu().numpy(), L.o1c[e]), f"W1 codes expert {e}"
+        assert np.array_equal(L.w1s[e].cpu().numpy(), L.o1s[e]), f"W1 scales expert {e}"
+        assert np.array_equal(L.w2c[e].cpu().numpy(), L.o2c[e]), f"W2 codes expert {e}"
+        assert np.array_equal(L.w2s[e].cpu().numpy(), L.o2s[e]), f"W2 scales expert {e}"
+    ref = oracle_forward(L, want_h=True)
+    r = _steps(L)
+    assert r["status"] == (0, 0)
+    assert np.array_equal(r["act_c"].cpu().numpy(), ref["act_codes"])
+    assert np.array_equal(r["act_s"].cpu().numpy(), ref["act_scales"])
+    assert np.array_equal(r["ids"].cpu().numpy(), ref["ids"])
+    np.testing.assert_allclose(r["w"].cpu().numpy(), ref["topk_w"], rtol=2e-6, atol=1e-7)
+    rc, ro, rs = oracle.permute(ref["ids"], wl.E)
+    assert np.array_equal(r["counts"].cpu().numpy(), rc)
+    assert np.array_equal(r["offsets"].cpu().numpy(), ro)
+    assert np.array_equal(r["ss"].cpu().numpy(), rs)
+    frac, hrel = _check_h(r, ref, wl.I)
+    assert frac < 0.02 and hrel < 0.02, (frac, hrel)
+    rel, mabs = out_errors(r["out"].double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    # the fused single call gives the same layer
+    out = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel2, mabs2 = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel2 <= OUT_REL_L2 and mabs2 <= OUT_MAX_ABS_OVER_RMS, (rel2, mabs2)
+    step_vs_fused = (out - r["out"]).abs().max().item() / max(r["out"].abs().max().item(), 1e-30)
+    assert step_vs_fused < 1e-5
+
+
+def test_prefill_full_size_sampled():
+    """8192-token prefill workload at full size, in the launch configuration the
+    benchmark times; the oracle evaluates a sample of tokens one by one."""
+    wl = W.WORKLOADS["prefill_mxfp8"]
+    logits, _ = W.draw_router_and_activations(wl, 0, "cuda")
+    rng = np.random.default_rng(0)
+    tokens = sorted(set([0, wl.T - 1] + rng.choice(wl.T, 14, replace=False).tolist()))
+    rid, _ = oracle.route_topk(logits.cpu().numpy(), wl.k)
+    need = set(int(e) for e in rid[tokens].ravel()) | {wl.E}
+    L = build_layer(wl, oracle_experts=need)
+    for e in sorted(need)[:4]:
+        assert np.array_equal(L.w1c[e].cpu().numpy(), L.o1c[e])
+        assert np.array_equal(L.w2c[e].cpu().numpy(), L.o2c[e])
+    ref = oracle_forward(L, tokens=tokens)
+    out = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    got = out[tokens].double().cpu().numpy()
+    rel, mabs = out_errors(got, ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    # bit-exact routing and permutation over the whole workload
+    assert np.array_equal(ref["ids"], rid)
+    r = _steps(L)
+    assert np.array_equal(r["ids"].cpu().numpy(), rid)
+    rc, ro, rs = oracle.permute(rid, wl.E)
+    assert np.array_equal(r["offsets"].cpu().numpy(), ro)
+    assert np.array_equal(r["ss"].cpu().numpy(), rs)
+    assert np.array_equal(r["act_c"].cpu().numpy(), ref["act_codes"])
+    # every token row is finite and the whole-layer output equals the step chain
+    assert torch.isfinite(out).all()
+    assert (out - r["out"]).abs().max().item() <= 1e-5 * r["out"].abs().max().item()
+
+
+def test_zero_tokens_is_a_noop():
+    wl = W.custom("empty", T=0, H=256, I=128, E=8, k=2)
+    ws = mx.alloc_workspace(1024)
+    x = torch.empty(0, 256, dtype=torch.bfloat16, device="cuda")
+    logits = torch.empty(0, 8, device="cuda")
+    out = torch.empty(0, 256, device="cuda")
+    w = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    mx.moe_forward(x, logits, w, w, "e4m3", wl.I, wl.k, out, ws)
+    torch.cuda.synchronize()
