@@ -1,0 +1,448 @@
+#!/usr/bin/env python3
+"""Benchmark of the MX block-scaled MoE expert layer on GB300.
+
+One step = one pass of the whole layer (activation quantisation, top-k
+routing, permutation, grouped gate/up GEMM + SwiGLU + requant, grouped down
+GEMM + combine) over one batch of the synthetic workload, on one GPU.  The
+default workload is the decode MXFP8 layer (T=32, H=4096, I=1536, 128 experts
+top-8 + 1 shared).  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+--impl reference times the CPU oracle (plain C, fp64) on a bounded sample of the
+same workload on this host's cores.  For N > 1 (torchrun) every rank runs an
+independent replica of the layer ("replicas only": the layer does not shard
+across GPUs here); throughput is the sum over ranks at the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_scaled_mx_gb300 import workload as W  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+MX8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode_mxfp8", choices=list(W.WORKLOADS))
+    ap.add_argument("--impl", default="mxmoe", choices=["mxmoe", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "fallback"
+    hbm, bf16, bf16s = FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            hbm = float(d.get("hbm_gbs", hbm))
+            bf16 = float(d.get("bf16_tflops", bf16))
+            bf16s = float(d.get("bf16_tflops_sustained", bf16s))
+            src = "measured"
+        except Exception:
+            pass
+    return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16s, "source": src}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ layer setup
+def build_gpu_layer(wl: W.Workload, dev):
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    fmt = mx.FORMATS[wl.fmt]
+    E1 = wl.E + 1
+    cdiv = 1 if fmt == mx.MX_E4M3 else 2
+    logits, x = W.draw_router_and_activations(wl, 0, dev)
+    w1c = torch.empty(E1, 2 * wl.I, wl.H // cdiv, dtype=torch.uint8, device=dev)
+    w1s = torch.empty(E1, 2 * wl.I, wl.H // 32, dtype=torch.uint8, device=dev)
+    w2c = torch.empty(E1, wl.H, wl.I // cdiv, dtype=torch.uint8, device=dev)
+    w2s = torch.empty(E1, wl.H, wl.I // 32, dtype=torch.uint8, device=dev)
+    for e in range(E1):
+        w1, w2 = W.draw_expert_weights(wl, e, 0, dev)
+        mx.mx_quantize_weights(w1, fmt, w1c[e], w1s[e])
+        mx.mx_quantize_weights(w2, fmt, w2c[e], w2s[e])
+        del w1, w2
+    layer = mx.MoELayer(w1c, w1s, w2c, w2s, fmt, wl.H, wl.I, wl.E, wl.k)
+    del w1c, w1s, w2c, w2s
+    torch.cuda.synchronize()
+    return layer, logits, x
+
+
+def weight_bytes_per_expert(wl: W.Workload):
+    elem = 1.0 if wl.fmt == "e4m3" else 0.5
+    w1 = 2 * wl.I * wl.H * elem + 2 * wl.I * wl.H / 32
+    w2 = wl.H * wl.I * elem + wl.H * wl.I / 32
+    return w1, w2
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "block_scaled_mx_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_tag: str, wl_name: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel_tag}_{wl_name}.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        if d.get("source_hash") != source_hash():
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+class OracleRunner:
+    """The CPU oracle on bounded samples of a workload: each call evaluates a
+    few tokens of it (quantised weights of the experts those tokens touch are
+    drawn and quantised on first use, untimed)."""
+
+    def __init__(self, wl: W.Workload):
+        import oracle
+
+        oracle.build()
+        self.oracle, self.wl = oracle, wl
+        logits, x = W.draw_router_and_activations(wl, 0, "cpu")
+        self.ids, _ = oracle.route_topk(logits.numpy(), wl.k)
+        self.fmt = oracle.E4M3 if wl.fmt == "e4m3" else oracle.E2M1
+        self.w = [[None] * (wl.E + 1) for _ in range(4)]
+        self.x_bits, self.lg = W.bf16_bits(x), logits.numpy()
+        self.next_token = 0
+        self.threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+
+    def call(self, n_tokens: int):
+        """Returns (tokens, seconds) of one timed oracle call."""
+        wl = self.wl
+        toks = sorted(set((self.next_token + i) % wl.T for i in range(n_tokens)))
+        self.next_token += n_tokens
+        for e in set(int(e) for e in self.ids[toks].ravel()) | {wl.E}:
+            if self.w[0][e] is None:
+                w1, w2 = W.draw_expert_weights(wl, e, 0, "cpu")
+                self.w[0][e], self.w[1][e] = self.oracle.quantize_f32(w1.numpy(), self.fmt)
+                self.w[2][e], self.w[3][e] = self.oracle.quantize_f32(w2.numpy(), self.fmt)
+        t0 = time.perf_counter()
+        self.oracle.moe_forward(self.x_bits, self.lg, wl.k, *self.w, self.fmt, wl.I, tokens=toks)
+        return len(toks), time.perf_counter() - t0
+
+    def rate(self, budget_s: float, n_tokens: int = 2):
+        done, spent, calls = 0, 0.0, 0
+        while spent < budget_s and calls < 256:
+            n, dt = self.call(n_tokens)
+            done, spent, calls = done + n, spent + dt, calls + 1
+        sample = (f"{done} tokens of the {self.wl.name} workload in {calls} oracle calls of {n_tokens} tokens "
+                  f"({spent:.1f} s; each call decodes the touched experts' weights to fp64 and runs fp64 GEMMs)")
+        return done / spent, sample
+
+
+# ------------------------------------------------------------------ main arms
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return
+    runner = OracleRunner(wl)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        n, dt = runner.call(1)
+        if i >= args.warmup:
+            per_step.append(dt / n)
+    sec_per_token = float(np.mean(per_step))
+    rate = 1.0 / sec_per_token
+    sample = (f"each step: the oracle on 1 token of the {wl.name} workload (tokens taken in order), "
+              f"{args.steps} timed steps after {args.warmup} warm-up")
+    line = {
+        "impl": "reference", "metric": "MoE layer tokens/s", "value": rate, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec_per_token * wl.T, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "shared_experts": 1, "weights": wl.fmt},
+        "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": runner.threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, wl, rank, world, local):
+    from block_scaled_mx_gb300 import build as B
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+        B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    layer, logits, x = build_gpu_layer(wl, dev)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    fmt = layer.fmt
+    stream = torch.cuda.current_stream()
+    # step-call buffers
+    act_c = torch.empty(T, H, dtype=torch.uint8, device=dev)
+    act_s = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    counts = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 2, dtype=torch.int32, device=dev)
+    ss = torch.empty(T * (k + 1), dtype=torch.int32, device=dev)
+    pws = mx.alloc_workspace(mx.moe_permute_workspace_size(T, E, k), dev)
+    gws = mx.alloc_workspace(mx.moe_gemm_workspace_size(T, H, I, E, k), dev)
+    h_c = torch.empty(T * (k + 1), I, dtype=torch.uint8, device=dev)
+    h_s = torch.empty(T * (k + 1), I // 32, dtype=torch.uint8, device=dev)
+    out = torch.empty(T, H, dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    nperm = 1 if T <= 256 else 2
+
+    def step(ev):
+        ev[0].record(stream)
+        mx.mx_quantize_act(x, act_c, act_s)
+        ev[1].record(stream)
+        mx.moe_route_topk(logits, k, ids, tw)
+        ev[2].record(stream)
+        mx.moe_permute(ids, E, counts, offsets, ss, pws)
+        out.zero_()
+        ev[3].record(stream)
+        mx.moe_grouped_gemm_swiglu(act_c, act_s, offsets, ss, layer.w1, fmt, T, H, I, E, k, h_c, h_s, gws)
+        ev[4].record(stream)
+        mx.moe_grouped_gemm_down_combine(h_c, h_s, offsets, ss, tw, layer.w2, fmt, T, H, I, E, k, out, gws)
+        ev[5].record(stream)
+
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(6)]  # noqa: E731
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step(mk())
+    torch.cuda.synchronize()
+    if mx.moe_get_status(pws) or mx.moe_get_status(gws):
+        raise RuntimeError("device status error during warm-up")
+    cnt = counts.cpu().numpy()
+    touched = int(np.count_nonzero(cnt))
+    w1b, w2b = weight_bytes_per_expert(wl)
+    evs = [mk() for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(1)          # L2 flush, outside the timed events
+            step(evs[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)])
+    step_ms = per.sum(1)
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms * 1e-3)
+
+    # ---- e2e through the public single call with host buffers
+    x_h = x.cpu().pin_memory()
+    lg_h = logits.cpu().pin_memory()
+    out_h = torch.empty(T, H, dtype=torch.float32).pin_memory()
+    x_d = torch.empty_like(x)
+    lg_d = torch.empty_like(logits)
+    out_d = torch.empty(T, H, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward(x_d, lg_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        layer.forward(x_d, lg_d, out_d)
+        out_h.copy_(out_d, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        t = torch.tensor([e2e], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(t.item())
+    if mx.moe_get_status(layer.workspace(T)):
+        raise RuntimeError("device status error in moe_forward")
+
+    if rank != 0:
+        return
+    pk = peaks()
+    gemm1_ms = float(per[:, 3].mean())
+    gemm2_ms = float(per[:, 4].mean())
+    # algorithmic bytes of the gate/up call: touched experts' W1 (codes + scales),
+    # the gathered activation rows read (and written once by the gather), h written
+    slots = T * (k + 1)
+    act_bytes = slots * H * (1 + 1 / 32)
+    g1_bytes = touched * w1b + 2 * slots * H + slots * H / 32 + slots * I * (1 + 1 / 32)
+    g2_bytes = touched * w2b + act_bytes * 0 + slots * I * (1 + 1 / 32) + 2 * T * H * 4
+    flops = 6.0 * slots * H * I
+    tc_peak = pk["bf16_tflops"] * MX8_OVER_BF16
+    hbm_peak = pk["hbm_gbs"]
+    bw = touched * (w1b + w2b)
+    layer_floor_ms = max(flops / (tc_peak * 1e12), bw / (hbm_peak * 1e9)) * 1e3
+    dominant_hbm = flops / (tc_peak * 1e12) < bw / (hbm_peak * 1e9)
+    if dominant_hbm:
+        achieved = g1_bytes / (gemm1_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": ncu_traffic("gemm1", wl.name), "kernel": "k_grouped_gemm (gate/up + SwiGLU + requant)",
+                "peak_source": pk["source"]}
+    else:
+        g1_flops = 4.0 * slots * H * I
+        achieved = g1_flops / (gemm1_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": achieved / tc_peak, "traffic": ncu_traffic("gemm1", wl.name),
+                "kernel": "k_grouped_gemm (gate/up + SwiGLU + requant)",
+                "peak_source": pk["source"] + " bf16 x2 (nominal MXFP8/bf16 ratio)"}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            runner = OracleRunner(wl)
+            rate, sample = runner.rate(args.cpu_budget_s)
+            cpu = {"value": rate, "unit": "tokens/s", "cores": runner.threads, "kind": "oracle", "sample": sample}
+        except Exception as exc:  # the GPU number stands without it
+            cpu = {"value": None, "unit": "tokens/s", "cores": None, "kind": "oracle", "sample": f"failed: {exc}"}
+    launches_per_step = 1 + 1 + nperm + 2 + 1
+    line = {
+        "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3" if wl.fmt == "e4m3" else "e2m1") + " x e4m3 -> f32 (MX block-scaled)",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k, "shared_experts": 1,
+                   "weights": "MXFP8 E4M3" if wl.fmt == "e4m3" else "MXFP4 E2M1",
+                   "activations": "MXFP8 E4M3", "l2": "flushed between steps (2x L2 write outside the timed events)",
+                   "parallelism": f"replicas x{world}", "sms": n_sm},
+        "roofline": roof,
+        "layer_roofline": {"floor_us": layer_floor_ms * 1e3, "frac": layer_floor_ms / ms,
+                           "touched_experts": touched, "weight_bytes": bw, "flops": flops,
+                           "bound": "hbm" if dominant_hbm else "tensor"},
+        "kernels_ms": {"quantize": float(per[:, 0].mean()), "topk": float(per[:, 1].mean()),
+                       "permute+zero": float(per[:, 2].mean()), "gateup_call": gemm1_ms, "down_call": gemm2_ms},
+        "e2e": {"value": world * T / (e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
+                "d2h_bytes_per_step": T * H * 4, "ms_per_step": e2e},
+        "cpu_baseline": cpu,
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_step * args.steps,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        run_gpu(args, wl, rank, world, local)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
