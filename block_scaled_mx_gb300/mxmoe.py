@@ -37,6 +37,7 @@ SIGNATURES = {
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
+    "moe_permute_no_alloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
     "moe_prepared_weight_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_prepare_weights": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "moe_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
@@ -133,6 +134,13 @@ def moe_permute(topk_ids, E, counts, offsets, sorted_slot, ws, stream=None):
     T, k = topk_ids.shape
     _check(lib().moe_permute(_ptr(topk_ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(sorted_slot), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_no_alloc(topk_ids, E, counts, offsets, sorted_slot, stream=None):
+    """moe_permute with the library's own static scratch (for callers that may not allocate)."""
+    T, k = topk_ids.shape
+    _check(lib().moe_permute_no_alloc(_ptr(topk_ids), T, E, k, _ptr(counts), _ptr(offsets), _ptr(sorted_slot),
+                                      _stream(stream)), "moe_permute_no_alloc")
 
 
 def moe_prepared_weight_bytes(E1, H, I, fmt, which) -> int:

@@ -119,6 +119,24 @@ MX_API size_t moe_permute_workspace_size(int T, int E, int k);
 MX_API int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
                 int32_t* sorted_slot, void* ws, size_t ws_bytes, mx_stream_t stream);
 
+/* moe_permute without a caller workspace.  The pages have no counterpart:
+ * this entry exists for callers that are not allowed to allocate device
+ * memory (for example a plugin whose host framework owns all device memory
+ * and forbids cudaMalloc in its enqueue path, or a serving loop that must not
+ * call cudaMalloc because it can synchronise the device).  It computes exactly
+ * what moe_permute computes, using a fixed 400 KiB scratch array inside the
+ * library that every GPU loading the library keeps until the process exits.
+ *  - Limit: the scratch moe_permute_workspace_size(T, E, k) reports must fit
+ *    in 400 KiB (T <= 8192, E <= 512, k <= 8 always fits); larger requests
+ *    return MX_ERR_WORKSPACE and enqueue nothing.
+ *  - The array is shared by every call on a device and keeps the last call's
+ *    contents; calls that overlap on the GPU race, so keep them on one stream.
+ *  - The first call on a device looks up the array's device address; make it
+ *    before any stream capture.  Device-side id errors are not reported.
+ *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call. */
+MX_API int moe_permute_no_alloc(const int32_t* topk_ids, int T, int E, int k, int32_t* counts,
+                                int32_t* offsets, int32_t* sorted_slot, mx_stream_t stream);
+
 /* Bytes of a prepared (kernel-layout) weight table.  which = 1: W1, the
  * gate/up projection [E1][2I][H] (rows 0..I-1 gate, I..2I-1 up); which = 2:
  * W2, the down projection [E1][H][I].  E1 = E + 1 experts (shared last). */
