@@ -52,7 +52,6 @@ struct ForwardWs {
   int32_t* sorted_slot;
   uint8_t* act_codes;
   uint8_t* act_scales;
-  uint8_t* act_sorted;
   uint8_t* h_codes;
   uint8_t* h_scales;
   size_t bytes;
@@ -77,7 +76,6 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
   f.sorted_slot = reinterpret_cast<int32_t*>(take(slots * 4));
   f.act_codes = take(static_cast<size_t>(T) * H);
   f.act_scales = take(static_cast<size_t>(T) * (H / 32));
-  f.act_sorted = take(slots * H);
   f.h_codes = take(slots * I);
   f.h_scales = take(slots * (I / 32));
   f.bytes = off;
@@ -86,12 +84,9 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
 
 int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const void* w1_prep, int fmt, int T, int H, int I, int E,
-              int k, uint8_t* h_codes, uint8_t* h_scales, int* status, uint8_t* act_sorted,
-              cudaStream_t s) {
+              int k, uint8_t* h_codes, uint8_t* h_scales, int* status, cudaStream_t s) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
-  cudaError_t e = launch_gather_rows(act_codes, T, H, sorted_slot, k, n_rows, act_sorted, status, s);
-  if (e != cudaSuccess) return MX_ERR_CUDA;
   GemmArgs a{};
   a.epi = 0;
   a.fmt = fmt;
@@ -101,7 +96,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.E = E;
   a.k = k;
   a.w_prep = w1_prep;
-  a.b_codes = act_sorted;
+  a.b_codes = act_codes;
   a.n_rows = n_rows;
   a.b_scales = act_scales;
   a.offsets = offsets;
@@ -230,7 +225,7 @@ int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int
 
 size_t moe_gemm_workspace_size(int T, int H, int I, int E, int k) {
   if (check_gemm_shape(T, H, I, E, k, MX_E4M3) != MX_OK) return 0;
-  return al256(256) + al256(static_cast<size_t>(T) * (k + 1) * H);
+  return al256(256);
 }
 
 int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
@@ -248,8 +243,7 @@ int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
   if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   return run_gemm1(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k, h_codes,
-                   h_scales, reinterpret_cast<int*>(w), w + al256(256),
-                   reinterpret_cast<cudaStream_t>(stream));
+                   h_scales, reinterpret_cast<int*>(w), reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
@@ -295,7 +289,7 @@ int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, co
   if (launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
     return MX_ERR_CUDA;
   st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s);
+                 f.h_codes, f.h_scales, f.perm.status, s);
   if (st != MX_OK) return st;
   return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
                    k, out, f.perm.status, s);

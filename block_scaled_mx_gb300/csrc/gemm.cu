@@ -218,33 +218,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ================================================================ producer
+    // Lane 0 arms each stage and issues the weight-block TMA loads and their
+    // scale-block bulk copies; the token rows come either as one 2-D box (down GEMM: h rows are contiguous)
+    // or as TMA gather4 loads of four token rows each, one per lane (gate/up:
+    // the tokens of an expert are scattered over the activation matrix).
     if (lane == 0) {
       prefetch_tensormap(&tm_a);
       prefetch_tensormap(&tm_b);
-      uint32_t it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
-        int rb0, rb1;
-        bool two;
-        if (p.epi == 0) {
-          rb0 = tl.m;
-          rb1 = p.RB / 2 + tl.m;
-          two = true;
-        } else {
-          rb0 = 2 * tl.m;
-          rb1 = 2 * tl.m + 1;
-          two = rb1 < p.RB;
+    }
+    const bool gather = p.epi == 0;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      int rb0, rb1;
+      bool two;
+      if (p.epi == 0) {
+        rb0 = tl.m;
+        rb1 = p.RB / 2 + tl.m;
+        two = true;
+      } else {
+        rb0 = 2 * tl.m;
+        rb1 = 2 * tl.m + 1;
+        two = rb1 < p.RB;
+      }
+      // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token)
+      const int n4 = gather ? (tl.rows + 3) / 4 : 0;
+      int tok[4] = {0, 0, 0, 0};
+      if (gather && lane < n4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = min(4 * lane + j, tl.rows - 1);
+          const int tt = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
+          if (tt < 0 || tt >= p.T) set_status(p.status, MX_ERR_DEVICE_ARG);
+          tok[j] = (tt < 0 || tt >= p.T) ? 0 : tt;
         }
-        const uint32_t bytes = (p.a_tx + 512u) * (two ? 2u : 1u) + static_cast<uint32_t>(p.bn) * 128u;
-        for (int kc = 0; kc < NK; ++kc, ++it) {
-          const int s = static_cast<int>(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t full = smem_u32(&sh.full[s]);
+      }
+      const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
+      const uint32_t bytes = (p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes;
+      for (int kc = 0; kc < NK; ++kc, ++it) {
+        const int s = static_cast<int>(it % S);
+        const uint32_t ph = (it / S) & 1u;
+        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t full = smem_u32(&sh.full[s]);
+        const uint32_t b_s = smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u);
+        if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
           uint8_t* a_s = base + p.off_a + static_cast<uint32_t>(s) * 32768u;
           uint8_t* sfa_s = base + p.off_sfa + static_cast<uint32_t>(s) * 1024u;
@@ -256,11 +277,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
             bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
           }
-          tma_load_2d(smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u), &tm_b,
-                      kc * 128, tl.p0, full);
+          if (!gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
+
         }
+        __syncwarp();
+        if (gather && lane < n4)
+          tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
+                      tok[3], full);
       }
-      // drain: every fill this thread armed has landed before the CTA exits
+    }
+    // drain: every fill this warp armed has landed before the CTA exits
+    if (lane == 0) {
       const uint32_t n_fills = it;
       for (int s = 0; s < S && static_cast<uint32_t>(s) < n_fills; ++s) {
         const uint32_t last = n_fills - 1 - ((n_fills - 1 - s) % S);
@@ -326,28 +353,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* sfbt = reinterpret_cast<uint32_t*>(base + p.off_sfbt);
     const int stride = p.sfbt_stride;
     const int K32 = p.K / 32;
+    const int tab = p.bn * NK;
+    auto table_entry = [&](const Tile& tl, int idx) -> uint32_t {
+      const int r = idx / NK, c = idx - r * NK;
+      if (r >= tl.rows) return 0x7F7F7F7Fu;
+      int src_row = tl.p0 + r;
+      if (p.epi == 0) {
+        src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
+        if (src_row < 0 || src_row >= p.T) {
+          set_status(p.status, MX_ERR_DEVICE_ARG);
+          src_row = 0;
+        }
+      }
+      return __ldg(reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32) + c);
+    };
     uint32_t it = 0, tj = 0;
     bool ok = true;
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tj) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
       // the previous tile's table has been consumed by all four warps
       if (!warp_wait_bar(sh, sh.sfbt_empty, (tj & 1u) ^ 1u, p.wait_limit_ns, p.status)) break;
-      for (int idx = sft; idx < p.bn * NK; idx += 128) {
+      for (int idx = sft; idx < tab; idx += 128) {
         const int r = idx / NK, c = idx - r * NK;
-        uint32_t v = 0x7F7F7F7Fu;
-        if (r < tl.rows) {
-          int src_row = tl.p0 + r;
-          if (p.epi == 0) {
-            const int slot = __ldg(&p.sorted_slot[tl.p0 + r]);
-            src_row = slot / (p.k + 1);
-            if (src_row < 0 || src_row >= p.T) {
-              set_status(p.status, MX_ERR_DEVICE_ARG);
-              src_row = 0;
-            }
-          }
-          v = __ldg(reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32) + c);
-        }
-        sfbt[r * stride + c] = v;
+        sfbt[r * stride + c] = table_entry(tl, idx);
       }
       mbar_arrive(smem_u32(sh.sfbt_full));
       if (!warp_wait_bar(sh, sh.sfbt_full, tj & 1u, p.wait_limit_ns, p.status)) break;
@@ -582,9 +610,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), static_cast<cuuint64_t>(a.n_rows)};
+    // gate/up: the activation matrix [T, H], gathered four token rows at a time
+    // (box one row high); down: the slot-ordered h rows [rows, I], one box per stage
+    const cuuint64_t b_rows = static_cast<cuuint64_t>(a.epi == 0 ? a.T : a.n_rows);
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), b_rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(p.bn)};
+    cuuint32_t box[2] = {128, a.epi == 0 ? 1u : static_cast<cuuint32_t>(p.bn)};
     cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.b_codes), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

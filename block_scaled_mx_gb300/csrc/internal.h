@@ -58,7 +58,8 @@ struct GemmArgs {
   int fmt;               // weight format (MX_E4M3 / MX_E2M1)
   int T, H, I, E, k;
   const void* w_prep;    // prepared weights
-  const uint8_t* b_codes;   // B operand rows [n_rows, K] (sorted order)
+  const uint8_t* b_codes;   // gate/up: activation codes [T, H] (rows gathered by token);
+                            // down: h codes [n_rows, I] in slot order
   int n_rows;               // T*(k+1)
   const uint8_t* b_scales;  // GEMM1: act scales [T, H/32] by token; GEMM2: h scales [rows, I/32]
   const int32_t* offsets;   // [E+2]

@@ -14,7 +14,8 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmxmoe.so")
+# MXMOE_LIB selects another build of the same library (e.g. a tuning variant)
+LIB_PATH = os.environ.get("MXMOE_LIB") or os.path.join(_HERE, "libmxmoe.so")
 
 MX_OK = 0
 MX_ERR_INVALID_ARG = 1

@@ -175,6 +175,10 @@ LAYER_CASES = {
     # wide (prefill) schedule with several ragged token tiles per expert
     "wide_e4m3": W.custom("wide_e4m3", T=1024, H=512, I=256, E=8, k=2, fmt="e4m3", zipf_bias=True),
     "wide_e2m1": W.custom("wide_e2m1", T=700, H=256, I=384, E=4, k=1, fmt="e2m1"),
+    # degenerate shapes: one token; a single routed expert; k = E
+    "one_token": W.custom("one_token", T=1, H=256, I=128, E=4, k=2, fmt="e4m3"),
+    "one_expert": W.custom("one_expert", T=5, H=128, I=128, E=1, k=1, fmt="e2m1"),
+    "k_equals_e": W.custom("k_equals_e", T=9, H=256, I=256, E=4, k=4, fmt="e4m3"),
 }
 
 
