@@ -41,6 +41,15 @@ int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
   return MX_OK;
 }
 
+// The narrow schedule gathers each tile's few token rows with TMA gather4; the
+// wide schedule first copies the activation rows into slot order (one row-gather
+// kernel) so that each stage's 128 token rows arrive as one TMA box.
+bool wide_schedule(int T, int E, int k) { return choose_bn(T, E, k) > 64; }
+
+size_t gather_bytes(int T, int H, int E, int k) {
+  return wide_schedule(T, E, k) ? al256(static_cast<size_t>(T) * (k + 1) * H) : 0;
+}
+
 // moe_forward workspace carve (status word first, shared with the permutation
 // scratch).
 struct ForwardWs {
@@ -52,6 +61,7 @@ struct ForwardWs {
   int32_t* sorted_slot;
   uint8_t* act_codes;
   uint8_t* act_scales;
+  uint8_t* act_sorted;
   uint8_t* h_codes;
   uint8_t* h_scales;
   size_t bytes;
@@ -76,6 +86,7 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
   f.sorted_slot = reinterpret_cast<int32_t*>(take(slots * 4));
   f.act_codes = take(static_cast<size_t>(T) * H);
   f.act_scales = take(static_cast<size_t>(T) * (H / 32));
+  f.act_sorted = take(gather_bytes(T, H, E, k));
   f.h_codes = take(slots * I);
   f.h_scales = take(slots * (I / 32));
   f.bytes = off;
@@ -84,10 +95,18 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
 
 int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const void* w1_prep, int fmt, int T, int H, int I, int E,
-              int k, uint8_t* h_codes, uint8_t* h_scales, int* status, cudaStream_t s) {
+              int k, uint8_t* h_codes, uint8_t* h_scales, int* status, uint8_t* act_sorted,
+              cudaStream_t s, int pdl = 0) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
+  a.bn = choose_bn(T, E, k);
+  a.gather4 = a.bn <= 64 ? 1 : 0;
+  a.pdl = a.gather4 ? pdl : 0;
+  if (!a.gather4) {
+    if (launch_gather_rows(act_codes, T, H, sorted_slot, k, n_rows, act_sorted, status, s) != cudaSuccess)
+      return MX_ERR_CUDA;
+  }
   a.epi = 0;
   a.fmt = fmt;
   a.T = T;
@@ -96,7 +115,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.E = E;
   a.k = k;
   a.w_prep = w1_prep;
-  a.b_codes = act_codes;
+  a.b_codes = a.gather4 ? act_codes : act_sorted;
   a.n_rows = n_rows;
   a.b_scales = act_scales;
   a.offsets = offsets;
@@ -104,14 +123,13 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.h_codes = h_codes;
   a.h_scales = h_scales;
   a.status = status;
-  a.bn = choose_bn(T, E, k);
   a.wait_limit_ns = g_wait_limit_ns;
   return cuda_status(launch_grouped_gemm(a, s));
 }
 
 int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const float* topk_w, const void* w2_prep, int fmt, int T,
-              int H, int I, int E, int k, float* out, int* status, cudaStream_t s) {
+              int H, int I, int E, int k, float* out, int* status, cudaStream_t s, int pdl = 0) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
@@ -131,6 +149,7 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.topk_w = topk_w;
   a.out = out;
   a.status = status;
+  a.pdl = pdl;
   a.bn = choose_bn(T, E, k);
   a.wait_limit_ns = g_wait_limit_ns;
   return cuda_status(launch_grouped_gemm(a, s));
@@ -225,7 +244,7 @@ int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int
 
 size_t moe_gemm_workspace_size(int T, int H, int I, int E, int k) {
   if (check_gemm_shape(T, H, I, E, k, MX_E4M3) != MX_OK) return 0;
-  return al256(256);
+  return al256(256) + gather_bytes(T, H, E, k);
 }
 
 int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
@@ -243,7 +262,7 @@ int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
   if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   return run_gemm1(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k, h_codes,
-                   h_scales, reinterpret_cast<int*>(w), reinterpret_cast<cudaStream_t>(stream));
+                   h_scales, reinterpret_cast<int*>(w), w + al256(256), reinterpret_cast<cudaStream_t>(stream));
 }
 
 int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
@@ -282,17 +301,37 @@ int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, co
   if (ws_bytes < moe_workspace_size(T, H, I, E, k, fmt)) return MX_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const ForwardWs f = carve_forward(ws, T, H, I, E, k);
-  if (launch_zero(out, static_cast<size_t>(T) * H * 4, s) != cudaSuccess) return MX_ERR_CUDA;
-  if (launch_quantize_act(x_bf16, static_cast<int64_t>(T) * H, f.act_codes, f.act_scales, s) != cudaSuccess)
-    return MX_ERR_CUDA;
-  if (launch_topk(logits, T, E, k, f.ids, f.topk_w, s) != cudaSuccess) return MX_ERR_CUDA;
-  if (launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
+  // Decode sizes run in three launches: the prologue (routing, quantisation,
+  // zeroing of out, permutation in its last block), then the two grouped GEMMs
+  // as programmatically dependent launches that set up while their predecessor
+  // drains.  Larger batches permute in their own chunked kernels.
+  const bool fused = T <= kPermuteChunk && !wide_schedule(T, E, k);
+  PrologueArgs pa{};
+  pa.x = static_cast<const uint4*>(x_bf16);
+  pa.n8 = static_cast<int64_t>(T) * H / 8;
+  pa.codes = reinterpret_cast<uint2*>(f.act_codes);
+  pa.scales = f.act_scales;
+  pa.logits = logits;
+  pa.T = T;
+  pa.E = E;
+  pa.k = k;
+  pa.ids = f.ids;
+  pa.topk_w = f.topk_w;
+  pa.out = reinterpret_cast<float4*>(out);
+  pa.n_out4 = static_cast<int64_t>(T) * H / 4;
+  pa.permute = fused ? 1 : 0;
+  pa.counts = f.counts;
+  pa.offsets = f.offsets;
+  pa.sorted_slot = f.sorted_slot;
+  pa.sc = f.perm;
+  if (launch_prologue(pa, s) != cudaSuccess) return MX_ERR_CUDA;
+  if (!fused && launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
     return MX_ERR_CUDA;
   st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                 f.h_codes, f.h_scales, f.perm.status, s);
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0);
   if (st != MX_OK) return st;
   return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
-                   k, out, f.perm.status, s);
+                   k, out, f.perm.status, s, 2);
 }
 
 int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <cstdint>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "internal.h"
@@ -66,6 +67,8 @@ struct GemmParams {
   uint32_t off_a, off_b, off_sfa, off_sfbt, off_meta, off_bar;
   uint32_t sf_col0;
   int sfbt_stride;  // words per row of the per-tile B scale table (NK + 1)
+  int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
+  int pdl;          // see GemmArgs::pdl
 };
 
 struct Tile {
@@ -159,7 +162,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- prologue: expert offsets, per-expert tile counts and their prefix
   const int E1 = p.E + 1;
-  for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = __ldg(&p.offsets[i]);
+  if (p.pdl == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.pdl != 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = p.offsets[i];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&sh.full[s]), 1);
@@ -226,9 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_a);
       prefetch_tensormap(&tm_b);
     }
-    const bool gather = p.epi == 0;
+    const bool gather = p.gather4 != 0;
     uint32_t it = 0;
     bool ok = true;
+    bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
       int rb0, rb1;
@@ -277,9 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
             bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
           }
-          if (!gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
-
         }
+        if (!b_ready) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          b_ready = true;
+        }
+        if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
         __syncwarp();
         if (gather && lane < n4)
           tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
@@ -369,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     uint32_t it = 0, tj = 0;
     bool ok = true;
+    if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tj) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
       // the previous tile's table has been consumed by all four warps
@@ -554,6 +564,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   p.sfbt_stride = p.NK + 1;
+  p.gather4 = a.gather4;
+  p.pdl = a.pdl;
   p.sf_col0 = 2u * static_cast<uint32_t>(p.acc_bufs) * static_cast<uint32_t>(p.bn);
 
   // shared memory plan
@@ -567,6 +579,10 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/;
   int stages = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
   if (stages > kMaxStages) stages = kMaxStages;
+  if (const char* env = std::getenv("MXMOE_STAGES")) {  // tuning override (only lowers)
+    const int v = std::atoi(env);
+    if (v >= 2 && v < stages) stages = v;
+  }
   const int tmem_room = static_cast<int>((kTmemCols - p.sf_col0) / kSfColsPerStage);
   if (stages > tmem_room) stages = tmem_room;
   if (stages < 2) return cudaErrorInvalidConfiguration;
@@ -610,12 +626,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
   {
-    // gate/up: the activation matrix [T, H], gathered four token rows at a time
-    // (box one row high); down: the slot-ordered h rows [rows, I], one box per stage
-    const cuuint64_t b_rows = static_cast<cuuint64_t>(a.epi == 0 ? a.T : a.n_rows);
+    // gather4: the activation matrix [T, H], four token rows at a time (box one
+    // row high); otherwise slot-ordered rows [n_rows, K], one bn-row box per stage
+    const cuuint64_t b_rows = static_cast<cuuint64_t>(p.gather4 ? a.T : a.n_rows);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), b_rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-    cuuint32_t box[2] = {128, a.epi == 0 ? 1u : static_cast<cuuint32_t>(p.bn)};
+    cuuint32_t box[2] = {128, p.gather4 ? 1u : static_cast<cuuint32_t>(p.bn)};
     cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.b_codes), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -631,8 +647,21 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       static_cast<long long>(p.NM) * (a.E + 1 + (a.n_rows + p.bn - 1) / p.bn);
   int grid = sm_count_gemm();
   if (bound < grid) grid = static_cast<int>(bound > 0 ? bound : 1);
-  k_grouped_gemm<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
-  return cudaGetLastError();
+  if (!a.pdl) {
+    k_grouped_gemm<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_grouped_gemm, p, tm_a, tm_b);
 }
 
 }  // namespace mxk

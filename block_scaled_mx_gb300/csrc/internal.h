@@ -32,6 +32,28 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
                            int32_t* offsets, int32_t* sorted_slot, const PermuteScratch& sc,
                            cudaStream_t s);
 
+// The fused layer's first launch: routing, activation quantisation and zeroing
+// of out over all blocks; with `permute` (T <= kPermuteChunk) the last block
+// also computes counts / offsets / sorted_slot.
+struct PrologueArgs {
+  const uint4* x;       // bf16 [T, H] as 16-byte groups
+  int64_t n8;           // T*H/8
+  uint2* codes;         // MXFP8 codes, 8 per group
+  uint8_t* scales;
+  const float* logits;
+  int T, E, k;
+  int32_t* ids;
+  float* topk_w;
+  float4* out;
+  int64_t n_out4;       // T*H/4
+  int permute;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* sorted_slot;
+  PermuteScratch sc;
+};
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
+
 // dst[p, :] = src[sorted_slot[p] / (k+1), :] for p < n_rows (rows of `row_bytes`).
 cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
                                const int32_t* sorted_slot, int k, int n_rows, uint8_t* dst,
@@ -58,8 +80,9 @@ struct GemmArgs {
   int fmt;               // weight format (MX_E4M3 / MX_E2M1)
   int T, H, I, E, k;
   const void* w_prep;    // prepared weights
-  const uint8_t* b_codes;   // gate/up: activation codes [T, H] (rows gathered by token);
-                            // down: h codes [n_rows, I] in slot order
+  const uint8_t* b_codes;   // gather4: activation codes [T, H] (rows gathered by token);
+                            // else rows [n_rows, K] already in slot order
+  int gather4;
   int n_rows;               // T*(k+1)
   const uint8_t* b_scales;  // GEMM1: act scales [T, H/32] by token; GEMM2: h scales [rows, I/32]
   const int32_t* offsets;   // [E+2]
@@ -71,6 +94,10 @@ struct GemmArgs {
   int* status;
   int bn;                   // N tile (32 or 128)
   uint64_t wait_limit_ns;
+  // programmatic dependent launch: 0 none; 1 the previous grid produced the
+  // offsets and the B rows (wait before anything); 2 the previous grid produced
+  // only the B rows and their scales (weights stream before the wait)
+  int pdl;
 };
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 

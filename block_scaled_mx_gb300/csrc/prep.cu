@@ -37,38 +37,43 @@ static unsigned grid_for(int64_t work_items, int threads, int per_sm) {
 // of 32.  Block amax over the bf16 magnitudes (integer max of the 15-bit
 // magnitude is monotonic), shared exponent from its bits, exact scaling by
 // 2^-s in fp32, then RNE/saturating E4M3 encoding.
+__device__ __forceinline__ void quantize_act_step(const uint4* __restrict__ x, int64_t n8, int64_t i,
+                                                  int lane, uint2* __restrict__ codes,
+                                                  uint8_t* __restrict__ scales) {
+  const bool valid = i < n8;
+  const uint4 v = valid ? __ldg(&x[i]) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t amax = 0;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    amax = max(amax, w[m] & 0x7FFFu);
+    amax = max(amax, (w[m] >> 16) & 0x7FFFu);
+  }
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int s = mx_block_exponent(amax << 16, 8);
+  const float p = pow2_neg(s);
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t c0 = enc_e4m3(__uint_as_float(w[m] << 16) * p);
+    const uint32_t c1 = enc_e4m3(__uint_as_float(w[m] & 0xFFFF0000u) * p);
+    packed[m >> 1] |= (c0 | (c1 << 8)) << ((m & 1) * 16);
+  }
+  if (valid) {
+    codes[i] = make_uint2(packed[0], packed[1]);
+    if ((lane & 3) == 0) scales[i >> 2] = static_cast<uint8_t>(s + 127);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_quantize_act(const uint4* __restrict__ x, int64_t n8,
                                                       uint2* __restrict__ codes,
                                                       uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - lane < n8;
-       i += stride) {
-    const bool valid = i < n8;
-    const uint4 v = valid ? __ldg(&x[i]) : make_uint4(0u, 0u, 0u, 0u);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t amax = 0;
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      amax = max(amax, w[m] & 0x7FFFu);
-      amax = max(amax, (w[m] >> 16) & 0x7FFFu);
-    }
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const int s = mx_block_exponent(amax << 16, 8);
-    const float p = pow2_neg(s);
-    uint32_t packed[2] = {0u, 0u};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t c0 = enc_e4m3(__uint_as_float(w[m] << 16) * p);
-      const uint32_t c1 = enc_e4m3(__uint_as_float(w[m] & 0xFFFF0000u) * p);
-      packed[m >> 1] |= (c0 | (c1 << 8)) << ((m & 1) * 16);
-    }
-    if (valid) {
-      codes[i] = make_uint2(packed[0], packed[1]);
-      if ((lane & 3) == 0) scales[i >> 2] = static_cast<uint8_t>(s + 127);
-    }
-  }
+       i += stride)
+    quantize_act_step(x, n8, i, lane, codes, scales);
 }
 
 cudaError_t launch_quantize_act(const void* x, int64_t n_elems, uint8_t* codes, uint8_t* scales,
@@ -133,11 +138,9 @@ cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, ui
 // among the logits not yet taken.  Lane j keeps round j's winner, so ids come
 // out in descending-logit order; softmax over the k winners in fp32.
 template <int PER>
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
-                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (t >= T) return;
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
+                                           int lane, int32_t* __restrict__ ids,
+                                           float* __restrict__ wout) {
   const float* row = logits + static_cast<int64_t>(t) * E;
   float v[PER];
 #pragma unroll
@@ -185,6 +188,14 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, 
   }
 }
 
+template <int PER>
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ logits, int T, int E, int k,
+                                              int32_t* __restrict__ ids, float* __restrict__ wout) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  topk_token<PER>(logits, t, E, k, threadIdx.x & 31, ids, wout);
+}
+
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                         cudaStream_t s) {
   if (T == 0) return cudaSuccess;
@@ -230,16 +241,19 @@ PermuteScratch permute_scratch_carve(void* ws, int T, int E, int k) {
   return sc;
 }
 
-__global__ void __launch_bounds__(kPermuteChunk) k_permute_count(
-    const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot, PermuteScratch sc,
-    int nchunks) {
-  extern __shared__ uint32_t bits[];  // [8 warps][E] lane masks, then E+2 ints of scan scratch
+// One chunk of pass 1 (and, for a single chunk, the whole permutation), run by
+// one block of kPermuteChunk threads.  `bits` is the dynamic shared scratch:
+// [8 warps][E] lane masks followed by E + 2 ints of scan space.
+__device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ ids, int T, int E,
+                                                    int k, int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets,
+                                                    int32_t* __restrict__ sorted_slot,
+                                                    const PermuteScratch& sc, int nchunks, int chunk,
+                                                    uint32_t* bits) {
   constexpr int kWarps = kPermuteChunk / 32;
   __shared__ int s_is_last;
   __shared__ int s_warp_tot[kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x;
   for (int i = tid; i < kWarps * E; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
   const int t = chunk * kPermuteChunk + tid;
@@ -249,7 +263,7 @@ __global__ void __launch_bounds__(kPermuteChunk) k_permute_count(
   for (int j = 0; j < 32; ++j) {
     my_e[j] = -1;
     if (j < k && valid) {
-      int e = ids[static_cast<int64_t>(t) * k + j];
+      int e = __ldcg(&ids[static_cast<int64_t>(t) * k + j]);
       if (e < 0 || e >= E) {
         set_status(sc.status, MX_ERR_DEVICE_ARG);
         e = -1;
@@ -347,6 +361,14 @@ __global__ void __launch_bounds__(kPermuteChunk) k_permute_count(
   }
 }
 
+__global__ void __launch_bounds__(kPermuteChunk) k_permute_count(
+    const int32_t* __restrict__ ids, int T, int E, int k, int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ sorted_slot, PermuteScratch sc,
+    int nchunks) {
+  extern __shared__ uint32_t bits[];
+  permute_count_block(ids, T, E, k, counts, offsets, sorted_slot, sc, nchunks, blockIdx.x, bits);
+}
+
 __global__ void __launch_bounds__(kPermuteChunk) k_permute_scatter(
     const int32_t* __restrict__ ids, int T, int E, int k, const int32_t* __restrict__ offsets,
     int32_t* __restrict__ sorted_slot, PermuteScratch sc) {
@@ -379,6 +401,60 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nchunks == 1) return e;
   k_permute_scatter<<<nchunks, kPermuteChunk, 0, s>>>(ids, T, E, k, offsets, sorted_slot, sc);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ fused prologue
+// The first launch of the fused layer: every block routes its share of tokens
+// (warp per token), quantises its share of x and zeroes its share of out; with
+// `permute` set, the last block to finish (threadfence + counter: nobody waits)
+// computes the whole permutation, which needs T <= kPermuteChunk.  It lets the
+// next grid (the gate/up GEMM, launched programmatically dependent) start its
+// set-up at once.
+template <int PER>
+__global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
+  extern __shared__ uint32_t bits[];
+  __shared__ int s_last;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int t = blockIdx.x * (kPermuteChunk / 32) + warp; t < a.T; t += gridDim.x * (kPermuteChunk / 32))
+    topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+  for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
+  for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!a.permute) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(a.sc.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  permute_count_block(a.ids, a.T, a.E, a.k, a.counts, a.offsets, a.sorted_slot, a.sc, 1, 0, bits);
+  if (tid == 0) *a.sc.done = 0u;  // ready for the next call
+}
+
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
+  const int64_t work = a.n8 > a.n_out4 ? a.n8 : a.n_out4;
+  int64_t blocks = (work + kPermuteChunk - 1) / kPermuteChunk;
+  const int64_t route_blocks = (a.T + kPermuteChunk / 32 - 1) / (kPermuteChunk / 32);
+  if (blocks < route_blocks) blocks = route_blocks;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const size_t smem = a.permute ? static_cast<size_t>(kPermuteChunk / 32) * a.E * 4 + static_cast<size_t>(a.E + 2) * 4 : 0;
+  const unsigned g = static_cast<unsigned>(blocks);
+  if (a.E <= 32) k_prologue<1><<<g, kPermuteChunk, smem, s>>>(a);
+  else if (a.E <= 128) k_prologue<4><<<g, kPermuteChunk, smem, s>>>(a);
+  else if (a.E <= 512) k_prologue<16><<<g, kPermuteChunk, smem, s>>>(a);
+  else {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k_prologue<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+    }
+    k_prologue<32><<<g, kPermuteChunk, smem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -257,3 +257,30 @@ def test_zero_tokens_is_a_noop():
     w = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
     mx.moe_forward(x, logits, w, w, "e4m3", wl.I, wl.k, out, ws)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["decode_mxfp8", "ragged_e2m1"])
+def test_forward_graph_capture(name):
+    """moe_forward issues only kernel launches (no host synchronisation, no
+    memset or allocation), so it can be captured in a CUDA graph and replayed;
+    the replay gives the eager result."""
+    wl = LAYER_CASES[name]
+    L = build_layer(wl, oracle_experts="none")
+    eager = L.layer.forward(L.x, L.logits).clone()
+    out = torch.empty_like(eager)
+    L.layer.forward(L.x, L.logits, out)           # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            L.layer.forward(L.x, L.logits, out)
+    torch.cuda.current_stream().wait_stream(s)
+    out.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    err = (out - eager).abs().max().item() / eager.abs().max().item()
+    assert err < 1e-5, err
