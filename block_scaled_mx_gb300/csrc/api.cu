@@ -19,18 +19,20 @@ inline size_t al256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
-// Token-row tile width of the grouped GEMMs: the narrow decode schedule keeps
-// two accumulator buffers per CTA so one tile's epilogue overlaps the next
-// tile's weight stream; the wide prefill schedule reuses each weight tile over
-// 128 token rows.  Chosen from the mean rows per expert, known on the host.
+// Token-row tile width of the grouped GEMMs, chosen from the mean rows per
+// expert (known on the host, no device read): the narrow decode schedule
+// (32 rows) streams weights with two accumulator buffers; the wide prefill
+// schedule reuses each weight tile over 96 token rows, the widest tile that
+// still leaves tensor memory for two accumulator buffers (so a tile's epilogue
+// overlaps the next tile's MMAs) and two stages of scale factors.
 int choose_bn(int T, int E, int k) {
   const char* env = std::getenv("MXMOE_BN");
   if (env) {
     const int v = std::atoi(env);
-    if (v == 32 || v == 64 || v == 128) return v;
+    if (v == 32 || v == 64 || v == 96 || v == 128) return v;
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
-  return mean_rows >= 48.0 ? 128 : 32;
+  return mean_rows >= 48.0 ? 96 : 32;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {

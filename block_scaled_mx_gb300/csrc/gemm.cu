@@ -45,7 +45,7 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpSf0 = 4;
 constexpr int kWarpEpi0 = 8;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfColsPerStage = 24;  // SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
+constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
 constexpr int kMaxStages = 8;
 
 struct GemmParams {
@@ -69,6 +69,7 @@ struct GemmParams {
   int sfbt_stride;  // words per row of the per-tile B scale table (NK + 1)
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
   int pdl;          // see GemmArgs::pdl
+  int kps;          // 128-wide K chunks per pipeline stage (1 or 2)
 };
 
 struct Tile {
@@ -261,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
-      const uint32_t bytes = (p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes;
-      for (int kc = 0; kc < NK; ++kc, ++it) {
+      const uint32_t bytes = ((p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes) * static_cast<uint32_t>(p.kps);
+      for (int ks = 0; ks < NK; ks += p.kps, ++it) {
         const int s = static_cast<int>(it % S);
         const uint32_t ph = (it / S) & 1u;
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
@@ -270,29 +271,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t full = smem_u32(&sh.full[s]);
-        const uint32_t b_s = smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u);
+        const uint32_t su = static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps);  // first chunk slot
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
-          uint8_t* a_s = base + p.off_a + static_cast<uint32_t>(s) * 32768u;
-          uint8_t* sfa_s = base + p.off_sfa + static_cast<uint32_t>(s) * 1024u;
-          const int blk0 = (tl.e * p.RB + rb0) * NK + kc;
-          tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
-          bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, 512u, full);
-          if (two) {
-            const int blk1 = (tl.e * p.RB + rb1) * NK + kc;
-            tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
-            bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
+          for (int u = 0; u < p.kps; ++u) {
+            const int kc = ks + u;
+            uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
+            uint8_t* sfa_s = base + p.off_sfa + (su + u) * 1024u;
+            const int blk0 = (tl.e * p.RB + rb0) * NK + kc;
+            tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
+            bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, 512u, full);
+            if (two) {
+              const int blk1 = (tl.e * p.RB + rb1) * NK + kc;
+              tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
+              bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
+            }
           }
         }
         if (!b_ready) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           b_ready = true;
         }
-        if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
-        __syncwarp();
-        if (gather && lane < n4)
-          tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
-                      tok[3], full);
+        for (int u = 0; u < p.kps; ++u) {
+          const int kc = ks + u;
+          const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.bn * 128u);
+          if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
+          __syncwarp();
+          if (gather && lane < n4)
+            tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
+                        tok[3], full);
+        }
       }
     }
     // drain: every fill this warp armed has landed before the CTA exits
@@ -308,6 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       const uint32_t afmt = p.afmt == MX_E4M3 ? kFmtE4M3 : kFmtE2M1;
+      const uint32_t sf_base = tbase + p.sf_col0;
+      const uint32_t sfa_base = smem_u32(base + p.off_sfa);
+      const uint32_t a_base = smem_u32(base + p.off_a);
+      const uint32_t b_base = smem_u32(base + p.off_b);
+      const uint32_t b_stride = static_cast<uint32_t>(p.bn) * 128u;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
         const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
@@ -320,7 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d0 = tbase + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
         const uint32_t d1 = tbase + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
-        for (int kc = 0; kc < NK; ++kc, ++it) {
+        uint32_t idesc[4];
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, 128, n_mma, kb, kb);
+        uint32_t accum = 0u;
+        for (int ks = 0; ks < NK; ks += p.kps, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
           if (!wait_bar(sh, &sh.full[s], ph, p.wait_limit_ns, p.status) ||
@@ -329,22 +346,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sf = tbase + p.sf_col0 + static_cast<uint32_t>(s) * kSfColsPerStage;
-          const uint32_t sfa_s = smem_u32(base + p.off_sfa + static_cast<uint32_t>(s) * 1024u);
-          tmem_cp_32x128b_warpx4(sf + 0u, smem_desc(sfa_s, 0, 128, kSwizzleNone));
-          if (two) tmem_cp_32x128b_warpx4(sf + 8u, smem_desc(sfa_s + 512u, 0, 128, kSwizzleNone));
-          const uint32_t a_s = smem_u32(base + p.off_a + static_cast<uint32_t>(s) * 32768u);
-          const uint32_t b_s = smem_u32(base + p.off_b + static_cast<uint32_t>(s) * p.bn * 128u);
+          const uint32_t su = static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps);
+          for (int u = 0; u < p.kps; ++u) {
+            const uint32_t slot = su + u;
+            const uint32_t sf = sf_base + slot * kSfColsPerChunk;
+            const uint32_t sfa_s = sfa_base + slot * 1024u;
+            tmem_cp_32x128b_warpx4(sf + 0u, smem_desc(sfa_s, 0, 128, kSwizzleNone));
+            if (two) tmem_cp_32x128b_warpx4(sf + 8u, smem_desc(sfa_s + 512u, 0, 128, kSwizzleNone));
+            const uint32_t a_lo = desc_lo_sw128(a_base + slot * 32768u);
+            const uint32_t b_lo = desc_lo_sw128(b_base + slot * b_stride);
 #pragma unroll
-          for (int kb = 0; kb < 4; ++kb) {
-            const uint32_t idesc = idesc_mx(afmt, kFmtE4M3, 128, n_mma, kb, kb);
-            const uint64_t bd = smem_desc(b_s + kb * 32, 16, 1024, kSwizzle128B);
-            const uint32_t acc = (kc | kb) != 0 ? 1u : 0u;
-            mma_mxf8f6f4(d0, smem_desc(a_s + kb * 32, 16, 1024, kSwizzle128B), bd, idesc, sf + 0u,
-                         sf + 16u, acc);
-            if (two)
-              mma_mxf8f6f4(d1, smem_desc(a_s + 16384u + kb * 32, 16, 1024, kSwizzle128B), bd, idesc,
-                           sf + 8u, sf + 16u, acc);
+            for (int kb = 0; kb < 4; ++kb) {
+              mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
+                              accum);
+              if (two)
+                mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb],
+                                sf + 8u, sf + 16u, accum);
+              accum = 1u;
+            }
           }
           mma_commit(smem_u32(&sh.empty[s]));
         }
@@ -362,20 +381,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* sfbt = reinterpret_cast<uint32_t*>(base + p.off_sfbt);
     const int stride = p.sfbt_stride;
     const int K32 = p.K / 32;
-    const int tab = p.bn * NK;
-    auto table_entry = [&](const Tile& tl, int idx) -> uint32_t {
-      const int r = idx / NK, c = idx - r * NK;
-      if (r >= tl.rows) return 0x7F7F7F7Fu;
-      int src_row = tl.p0 + r;
-      if (p.epi == 0) {
-        src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
-        if (src_row < 0 || src_row >= p.T) {
-          set_status(p.status, MX_ERR_DEVICE_ARG);
-          src_row = 0;
-        }
-      }
-      return __ldg(reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32) + c);
-    };
     uint32_t it = 0, tj = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -383,29 +388,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
       // the previous tile's table has been consumed by all four warps
       if (!warp_wait_bar(sh, sh.sfbt_empty, (tj & 1u) ^ 1u, p.wait_limit_ns, p.status)) break;
-      for (int idx = sft; idx < tab; idx += 128) {
-        const int r = idx / NK, c = idx - r * NK;
-        sfbt[r * stride + c] = table_entry(tl, idx);
+      // one row per thread: its token is looked up once, then the row's NK scale
+      // words are fetched with independent 16-byte loads (a loop of dependent
+      // slot -> token -> scale loads here cost tens of microseconds per tile)
+      for (int r = sft; r < p.bn; r += 128) {
+        if (r >= tl.rows) {
+          for (int c = 0; c < NK; ++c) sfbt[r * stride + c] = 0x7F7F7F7Fu;
+          continue;
+        }
+        int src_row = tl.p0 + r;
+        if (p.epi == 0) {
+          src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
+          if (src_row < 0 || src_row >= p.T) {
+            set_status(p.status, MX_ERR_DEVICE_ARG);
+            src_row = 0;
+          }
+        }
+        const uint8_t* srow = p.b_scales + static_cast<size_t>(src_row) * K32;
+        if ((NK & 3) == 0) {
+          uint4 v[8];
+          for (int c0 = 0; c0 < NK; c0 += 32) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (c0 + 4 * u < NK) v[u] = __ldg(reinterpret_cast<const uint4*>(srow) + (c0 / 4 + u));
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              if (c0 + 4 * u < NK) {
+                uint32_t* d = sfbt + r * stride + c0 + 4 * u;
+                d[0] = v[u].x;
+                d[1] = v[u].y;
+                d[2] = v[u].z;
+                d[3] = v[u].w;
+              }
+          }
+        } else {
+          for (int c = 0; c < NK; ++c) sfbt[r * stride + c] = __ldg(reinterpret_cast<const uint32_t*>(srow) + c);
+        }
       }
       mbar_arrive(smem_u32(sh.sfbt_full));
       if (!warp_wait_bar(sh, sh.sfbt_full, tj & 1u, p.wait_limit_ns, p.status)) break;
-      for (int kc = 0; kc < NK; ++kc, ++it) {
+      for (int ks = 0; ks < NK; ks += p.kps, ++it) {
         const int s = static_cast<int>(it % S);
         const uint32_t ph = (it / S) & 1u;
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
           ok = false;
           break;
         }
-        uint32_t w[4];
+        for (int u = 0; u < p.kps; ++u) {
+          uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = 32 * j + lane;
-          w[j] = r < p.bn ? sfbt[r * stride + kc] : 0x7F7F7F7Fu;
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + lane;
+            w[j] = r < p.bn ? sfbt[r * stride + ks + u] : 0x7F7F7F7Fu;
+          }
+          const uint32_t col = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 +
+                               (static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps) + u) * kSfColsPerChunk + 16u;
+          __syncwarp();
+          tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
         }
-        const uint32_t col = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 +
-                             static_cast<uint32_t>(s) * kSfColsPerStage + 16u;
-        __syncwarp();
-        tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -431,24 +471,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.epi == 0) {
         const int i = tl.m * 128 + 32 * q + lane;
         const int I32 = p.I / 32;
+        // 16 columns at a time, each step over all 16 so that the per-column
+        // chains (SwiGLU, warp amax, exponent, encode) overlap
         for (int c0 = 0; c0 < tl.rows; c0 += 16) {
           uint32_t g[16], u[16];
+          __syncwarp();
           tmem_ld_32x32b_x16(d0 + c0, g);
           tmem_ld_32x32b_x16(d1 + c0, u);
           tmem_ld_wait();
+          float h[16];
+          uint32_t amax[16];
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const float gv = __uint_as_float(g[cc]);
+            h[cc] = gv / (1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
+            amax[cc] = __float_as_uint(h[cc]) & 0x7FFFFFFFu;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) amax[cc] = __reduce_max_sync(0xffffffffu, amax[cc]);
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) {
             const int n = c0 + cc;
-            if (n >= tl.rows) break;
-            const float gv = __uint_as_float(g[cc]);
-            const float uv = __uint_as_float(u[cc]);
-            const float h = gv / (1.0f + __expf(-gv)) * uv;
-            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(h) & 0x7FFFFFFFu);
-            const int s = mx_block_exponent(amax, 8);
-            const uint32_t code = enc_e4m3(h * pow2_neg(s));
-            const size_t row = static_cast<size_t>(tl.p0 + n);
-            p.h_codes[row * p.I + i] = static_cast<uint8_t>(code);
-            if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>(s + 127);
+            const int s = mx_block_exponent(amax[cc], 8);
+            const uint32_t code = enc_e4m3(h[cc] * pow2_neg(s));
+            if (n < tl.rows) {
+              const size_t row = static_cast<size_t>(tl.p0 + n);
+              p.h_codes[row * p.I + i] = static_cast<uint8_t>(code);
+              if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>(s + 127);
+            }
           }
         }
       } else {
@@ -549,7 +599,14 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.RB = rows / 128;
   p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
   p.bn = a.bn;
-  p.acc_bufs = a.bn <= 64 ? 2 : 1;
+  p.kps = ((p.K / 128) % 2 == 0) ? 2 : 1;
+  if (const char* env = std::getenv("MXMOE_KPS")) {
+    const int v = std::atoi(env);
+    if (v == 1 || (v == 2 && (p.K / 128) % 2 == 0)) p.kps = v;
+  }
+  // two accumulator buffers (the epilogue of one tile overlaps the next tile's
+  // MMAs) whenever they leave tensor memory for two stages of scale factors
+  p.acc_bufs = (4u * static_cast<uint32_t>(a.bn) + 2u * kSfColsPerChunk * p.kps <= kTmemCols) ? 2 : 1;
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
   const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt);
@@ -564,6 +621,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   p.sfbt_stride = p.NK + 1;
+  // Two 128-wide K chunks per pipeline stage (set above): the fixed per-stage
+  // costs of the single MMA-issuing thread (barrier waits, fences, scale
+  // copies, commit) are then paid once per 256 K.
   p.gather4 = a.gather4;
   p.pdl = a.pdl;
   p.sf_col0 = 2u * static_cast<uint32_t>(p.acc_bufs) * static_cast<uint32_t>(p.bn);
@@ -571,7 +631,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   // shared memory plan
   const uint32_t sfbt_bytes = (static_cast<uint32_t>(p.bn) * p.sfbt_stride * 4u + 1023u) & ~1023u;
   const uint32_t meta_bytes = (static_cast<uint32_t>(a.E + 2) * 8u + 127u) & ~127u;
-  const uint32_t per_stage = 32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u;
+  const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u) * static_cast<uint32_t>(p.kps);
   int dev = 0;
   cudaGetDevice(&dev);
   int max_smem = 0;
@@ -583,17 +643,17 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     const int v = std::atoi(env);
     if (v >= 2 && v < stages) stages = v;
   }
-  const int tmem_room = static_cast<int>((kTmemCols - p.sf_col0) / kSfColsPerStage);
+  const int tmem_room = static_cast<int>((kTmemCols - p.sf_col0) / (kSfColsPerChunk * p.kps));
   if (stages > tmem_room) stages = tmem_room;
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
   uint32_t off = 0;
   p.off_a = off;
-  off += static_cast<uint32_t>(stages) * 32768u;
+  off += static_cast<uint32_t>(stages * p.kps) * 32768u;
   p.off_b = off;
-  off += static_cast<uint32_t>(stages) * p.bn * 128u;
+  off += static_cast<uint32_t>(stages * p.kps) * p.bn * 128u;
   p.off_sfa = off;
-  off += static_cast<uint32_t>(stages) * 1024u;
+  off += static_cast<uint32_t>(stages * p.kps) * 1024u;
   p.off_sfbt = off;
   off += sfbt_bytes;
   p.off_meta = off;

@@ -145,6 +145,29 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
       : "memory");
 }
+// Same MMA with the two shared-memory descriptors given as their low 32-bit
+// halves and one shared high half (stride, version, swizzle): the issuing
+// thread then spends one add per operand per K step instead of rebuilding
+// 64-bit descriptors.
+__device__ __forceinline__ void mma_mxf8f6f4_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                uint32_t desc_hi, uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 ad, {%1, %7};\n\t"
+      "mov.b64 bd, {%2, %7};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], ad, bd, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem), "r"(desc_hi)
+      : "memory");
+}
+// Low / high halves of the K-major, 128-byte-swizzled operand descriptor with
+// 8-row groups 1024 bytes apart (see smem_desc).
+__device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t addr) {
+  return ((addr >> 4) & 0x3FFFu) | (1u << 16);
+}
+constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // 128-byte swizzle
+
 // Arrive (once) on an mbarrier when every previously issued tcgen05 async
 // operation of this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

@@ -284,3 +284,16 @@ def test_forward_graph_capture(name):
     assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
     err = (out - eager).abs().max().item() / eager.abs().max().item()
     assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("name,kps", [("tiny", "2"), ("decode_mxfp8", "2"), ("decode_mxfp4", "1")])
+def test_layer_parity_other_stage_shape(name, kps, monkeypatch):
+    """The narrow schedule with the other number of K chunks per pipeline stage."""
+    monkeypatch.setenv("MXMOE_KPS", kps)
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle_forward(L)
+    out = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
