@@ -43,7 +43,7 @@ MX8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_mxfp8", choices=list(W.WORKLOADS))
     ap.add_argument("--impl", default="mxmoe", choices=["mxmoe", "reference"])
@@ -81,16 +81,19 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    PERIOD_MS = 20
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []          # (arrival time, csv line)
+        self.window = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
         except Exception:
@@ -99,7 +102,12 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """The timed region, in perf_counter seconds: only samples taken inside it
+        (or, when it is shorter than one period, the ones next to it) count."""
+        self.window = (t0, t1)
 
     def __exit__(self, *a):
         if self.proc:
@@ -112,7 +120,15 @@ class ClockSampler:
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        lines = self.lines
+        if self.window is not None:
+            t0, t1 = self.window
+            pad = 1.5 * self.PERIOD_MS * 1e-3
+            inside = [ln for t, ln in lines if t0 <= t <= t1 + pad]
+            lines = inside or [ln for t, ln in lines if t0 - pad <= t <= t1 + 2 * pad]
+        else:
+            lines = [ln for _, ln in lines]
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -320,6 +336,7 @@ def run_gpu(args, wl, rank, world, local):
         layer.forward(x, logits, out_f)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        time.sleep(0.3)             # the sampler's first lines arrive before the timed region
         t_wall0 = time.perf_counter()
         for i in range(args.steps):
             # (a) the layer through the fused single call: the step time
@@ -332,7 +349,10 @@ def run_gpu(args, wl, rank, world, local):
             flush.fill_(1)
             step(evs[i])
         torch.cuda.synchronize()
-        t_wall = time.perf_counter() - t_wall0
+        t_wall1 = time.perf_counter()
+        t_wall = t_wall1 - t_wall0
+        clk.mark(t_wall0, t_wall1)
+        time.sleep(3 * ClockSampler.PERIOD_MS * 1e-3)
     if world > 1:
         torch.distributed.barrier()
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)])
