@@ -20,19 +20,23 @@ inline size_t al256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; }
 
 // Token-row tile width of the grouped GEMMs, chosen from the mean rows per
-// expert (known on the host, no device read): the narrow decode schedule
-// (32 rows) streams weights with two accumulator buffers; the wide prefill
-// schedule reuses each weight tile over 96 token rows, the widest tile that
-// still leaves tensor memory for two accumulator buffers (so a tile's epilogue
-// overlaps the next tile's MMAs) and two stages of scale factors.
-int choose_bn(int T, int E, int k) {
-  const char* env = std::getenv("MXMOE_BN");
+// expert (known on the host, no device read).  The narrow decode schedule
+// (32 rows) streams weights with two accumulator buffers.  The wide prefill
+// schedule reuses each weight tile over many token rows: 192 for the gate/up
+// GEMM (one accumulator buffer: a block-scaled MMA costs about the same issue
+// time for any N up to 192, so doubling N over 96 outweighs the epilogue no
+// longer overlapping the MMAs) and 96 for the down GEMM, whose atomic combine
+// epilogue is too long to leave un-overlapped (two buffers).
+// `which`: 0 gate/up, 1 down.
+int choose_bn(int T, int E, int k, int which) {
+  const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
   if (env) {
     const int v = std::atoi(env);
-    if (v == 32 || v == 64 || v == 96 || v == 128) return v;
+    if (v >= 32 && v <= 224 && v % 32 == 0) return v;
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
-  return mean_rows >= 48.0 ? 96 : 32;
+  if (mean_rows < 48.0) return 32;
+  return which == 0 ? 192 : 96;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
@@ -46,7 +50,7 @@ int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
 // The narrow schedule gathers each tile's few token rows with TMA gather4; the
 // wide schedule first copies the activation rows into slot order (one row-gather
 // kernel) so that each stage's 128 token rows arrive as one TMA box.
-bool wide_schedule(int T, int E, int k) { return choose_bn(T, E, k) > 64; }
+bool wide_schedule(int T, int E, int k) { return choose_bn(T, E, k, 0) > 64; }
 
 size_t gather_bytes(int T, int H, int E, int k) {
   return wide_schedule(T, E, k) ? al256(static_cast<size_t>(T) * (k + 1) * H) : 0;
@@ -102,7 +106,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
-  a.bn = choose_bn(T, E, k);
+  a.bn = choose_bn(T, E, k, 0);
   a.gather4 = a.bn <= 64 ? 1 : 0;
   a.pdl = a.gather4 ? pdl : 0;
   if (!a.gather4) {
@@ -152,7 +156,7 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.out = out;
   a.status = status;
   a.pdl = pdl;
-  a.bn = choose_bn(T, E, k);
+  a.bn = choose_bn(T, E, k, 1);
   a.wait_limit_ns = g_wait_limit_ns;
   return cuda_status(launch_grouped_gemm(a, s));
 }

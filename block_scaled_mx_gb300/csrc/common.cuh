@@ -30,23 +30,14 @@ __device__ __forceinline__ float pow2_neg(int s) {
   return __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
 }
 
-// E4M3 code of q (finite, |q| < 512 after block scaling): round to nearest
-// even on the E4M3 grid (subnormal spacing 2^-9 below 2^-6), saturate at 448
-// (0x7E), keep the sign of q (so a negative value rounding to zero is 0x80).
-__device__ __forceinline__ uint32_t enc_e4m3(float q) {
-  const uint32_t u = __float_as_uint(q);
-  const uint32_t sign = (u >> 24) & 0x80u;
-  const uint32_t a = u & 0x7FFFFFFFu;
-  uint32_t code;
-  if (a >= 0x43E00000u) {            // >= 448
-    code = 0x7Eu;
-  } else if (a < 0x3C800000u) {      // < 2^-6: code = round(a / 2^-9), 0..8
-    code = static_cast<uint32_t>(__float2int_rn(__uint_as_float(a) * 512.0f));
-  } else {                           // normal: keep 3 mantissa bits, ties to even
-    const uint32_t r = (a + 0x7FFFFu + ((a >> 20) & 1u)) >> 20;
-    code = r - 960u;                 // (biased fp32 exponent - 120) << 3 | mantissa
-  }
-  return sign | code;
+// E4M3 codes of two block-scaled values (finite) with the hardware conversion:
+// round to nearest even on the E4M3 grid (subnormal spacing 2^-9 below 2^-6),
+// saturate at 448 (0x7E), keep the sign (a negative value rounding to zero is
+// 0x80).  The code of `lo` is in bits 0..7, that of `hi` in bits 8..15.
+__device__ __forceinline__ uint32_t enc_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // E2M1 code of q (finite, |q| < 8): magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6;

@@ -15,7 +15,7 @@
 // one CTA per SM; per-expert token counts are read from the device-side
 // permutation offsets, so nothing waits on the host.
 //
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
 //               unpacked to the 16-byte-aligned form by the TMA), their
 //               512-byte scale blocks (bulk copy), token rows (tensor map)
@@ -23,8 +23,9 @@
 //               scales and tcgen05.mma.kind::mxf8f6f4.block_scale
 //   warps 4-7   token-row scale staging: tcgen05.st of the B scale factors
 //               into every TMEM lane quarter
-//   warps 8-11  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
-//               MXFP8 re-quantisation or weighted combine
+//   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
+//               MXFP8 re-quantisation or weighted combine; warps w and w + 4
+//               share a TMEM lane quarter and take alternate column chunks
 // Every wait is bounded (wall clock); a wait that runs out sets
 // MX_ERR_TIMEOUT in the status word and every role unwinds.
 #include <cuda.h>
@@ -39,11 +40,12 @@
 
 namespace mxk {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kWarpTma = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpSf0 = 4;
 constexpr int kWarpEpi0 = 8;
+constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
 constexpr int kMaxStages = 8;
@@ -174,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.acc_full[a]), 1);
-      mbar_init(smem_u32(&sh.acc_empty[a]), 4);
+      mbar_init(smem_u32(&sh.acc_empty[a]), kEpiWarps);
     }
     mbar_init(smem_u32(sh.drain), 1);
     mbar_init(smem_u32(sh.sfbt_full), 128);
@@ -233,7 +235,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_b);
     }
     const bool gather = p.gather4 != 0;
-    uint32_t it = 0;
+    // ring position kept incrementally (no division by the runtime stage count)
+    const uint32_t S_ = static_cast<uint32_t>(S);
+    const int kps = p.kps;
+    const unsigned long long lim = p.wait_limit_ns;
+    int* const status = p.status;
+    uint32_t it = 0, rs = 0, rph = 0;
     bool ok = true;
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -262,19 +269,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
-      const uint32_t bytes = ((p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes) * static_cast<uint32_t>(p.kps);
-      for (int ks = 0; ks < NK; ks += p.kps, ++it) {
-        const int s = static_cast<int>(it % S);
-        const uint32_t ph = (it / S) & 1u;
-        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
+      const uint32_t bytes = ((p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes) * static_cast<uint32_t>(kps);
+      for (int ks = 0; ks < NK; ks += kps) {
+        const uint32_t s = rs, ph = rph;
+        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
         }
         const uint32_t full = smem_u32(&sh.full[s]);
-        const uint32_t su = static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps);  // first chunk slot
+        const uint32_t su = s * static_cast<uint32_t>(kps);  // first chunk slot
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
-          for (int u = 0; u < p.kps; ++u) {
+          for (int u = 0; u < kps; ++u) {
             const int kc = ks + u;
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
             uint8_t* sfa_s = base + p.off_sfa + (su + u) * 1024u;
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("griddepcontrol.wait;" ::: "memory");
           b_ready = true;
         }
-        for (int u = 0; u < p.kps; ++u) {
+        for (int u = 0; u < kps; ++u) {
           const int kc = ks + u;
           const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.bn * 128u);
           if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
@@ -300,6 +306,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (gather && lane < n4)
             tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
                         tok[3], full);
+        }
+        ++it;  // fills armed
+        if (++rs == S_) {
+          rs = 0;
+          rph ^= 1u;
         }
       }
     }
@@ -314,22 +325,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, tcount = 0;
+      // everything the issue loop needs lives in registers, and the ring and
+      // accumulator positions advance incrementally: the single issuing thread's
+      // per-stage latency (divisions, parameter reloads) is MMA issue time lost
+      const uint32_t S_ = static_cast<uint32_t>(S);
+      const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
+      const unsigned long long lim = p.wait_limit_ns;
+      int* const status = p.status;
+      const int NKs = NK / p.kps;  // stages per tile
+      uint32_t rs = 0, rph = 0, ab = 0, aph = 0;
       const uint32_t afmt = p.afmt == MX_E4M3 ? kFmtE4M3 : kFmtE2M1;
       const uint32_t sf_base = tbase + p.sf_col0;
       const uint32_t sfa_base = smem_u32(base + p.off_sfa);
       const uint32_t a_base = smem_u32(base + p.off_a);
       const uint32_t b_base = smem_u32(base + p.off_b);
-      const uint32_t b_stride = static_cast<uint32_t>(p.bn) * 128u;
+      const uint32_t b_stride16 = static_cast<uint32_t>(p.bn) * (128u >> 4);
+      const uint32_t kps = static_cast<uint32_t>(p.kps);
+      // descriptors of slot 0 (start address field is addr >> 4; slots add to it)
+      const uint64_t sfa_desc0 = smem_desc(sfa_base, 0, 128, kSwizzleNone);
+      const uint32_t a_lo0 = desc_lo_sw128(a_base);
+      const uint32_t b_lo0 = desc_lo_sw128(b_base);
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
         const bool two = p.epi == 0 || (2 * tl.m + 1 < p.RB);
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
-        const uint32_t ab = tcount % static_cast<uint32_t>(p.acc_bufs);
-        const uint32_t aph = (tcount / static_cast<uint32_t>(p.acc_bufs)) & 1u;
-        if (!wait_bar(sh, &sh.acc_empty[ab], aph ^ 1u, p.wait_limit_ns, p.status)) break;
+        if (!wait_bar(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
         tc_fence_after();
         const uint32_t d0 = tbase + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
         const uint32_t d1 = tbase + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
@@ -337,38 +359,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, 128, n_mma, kb, kb);
         uint32_t accum = 0u;
-        for (int ks = 0; ks < NK; ks += p.kps, ++it) {
-          const int s = static_cast<int>(it % S);
-          const uint32_t ph = (it / S) & 1u;
-          if (!wait_bar(sh, &sh.full[s], ph, p.wait_limit_ns, p.status) ||
-              !wait_bar(sh, &sh.sfb_ready[s], ph, p.wait_limit_ns, p.status)) {
+        for (int ks = 0; ks < NKs; ++ks) {
+          const uint32_t s = rs, ph = rph;
+          if (++rs == S_) {
+            rs = 0;
+            rph ^= 1u;
+          }
+          if (!wait_bar(sh, &sh.full[s], ph, lim, status) || !wait_bar(sh, &sh.sfb_ready[s], ph, lim, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t su = static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps);
-          for (int u = 0; u < p.kps; ++u) {
-            const uint32_t slot = su + u;
+          uint32_t slot = s * kps;
+          for (uint32_t u = 0; u < kps; ++u, ++slot) {
             const uint32_t sf = sf_base + slot * kSfColsPerChunk;
-            const uint32_t sfa_s = sfa_base + slot * 1024u;
-            tmem_cp_32x128b_warpx4(sf + 0u, smem_desc(sfa_s, 0, 128, kSwizzleNone));
-            if (two) tmem_cp_32x128b_warpx4(sf + 8u, smem_desc(sfa_s + 512u, 0, 128, kSwizzleNone));
-            const uint32_t a_lo = desc_lo_sw128(a_base + slot * 32768u);
-            const uint32_t b_lo = desc_lo_sw128(b_base + slot * b_stride);
+            const uint64_t sfa_d = sfa_desc0 + (static_cast<uint64_t>(slot * (1024u >> 4)));
+            const uint32_t a_lo = a_lo0 + slot * (32768u >> 4);
+            const uint32_t b_lo = b_lo0 + slot * b_stride16;
+            tmem_cp_32x128b_warpx4(sf + 0u, sfa_d);
+            if (two) {
+              tmem_cp_32x128b_warpx4(sf + 8u, sfa_d + (512u >> 4));
 #pragma unroll
-            for (int kb = 0; kb < 4; ++kb) {
-              mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
-                              accum);
-              if (two)
+              for (int kb = 0; kb < 4; ++kb) {
+                mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
+                                accum);
                 mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb],
                                 sf + 8u, sf + 16u, accum);
-              accum = 1u;
+                accum = 1u;
+              }
+            } else {
+#pragma unroll
+              for (int kb = 0; kb < 4; ++kb) {
+                mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
+                                accum);
+                accum = 1u;
+              }
             }
           }
           mma_commit(smem_u32(&sh.empty[s]));
         }
         if (!ok) break;
         mma_commit(smem_u32(&sh.acc_full[ab]));
+        if (++ab == acc_bufs) {
+          ab = 0;
+          aph ^= 1u;
+        }
       }
       // every MMA this thread issued has completed before TMEM is released
       mma_commit(smem_u32(sh.drain));
@@ -381,7 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* sfbt = reinterpret_cast<uint32_t*>(base + p.off_sfbt);
     const int stride = p.sfbt_stride;
     const int K32 = p.K / 32;
-    uint32_t it = 0, tj = 0;
+    const uint32_t S_ = static_cast<uint32_t>(S);
+    const int kps = p.kps, bn = p.bn;
+    const unsigned long long lim = p.wait_limit_ns;
+    int* const status = p.status;
+    const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 + 16u;
+    uint32_t rs = 0, rph = 0, tj = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tj) {
@@ -427,24 +467,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_arrive(smem_u32(sh.sfbt_full));
       if (!warp_wait_bar(sh, sh.sfbt_full, tj & 1u, p.wait_limit_ns, p.status)) break;
-      for (int ks = 0; ks < NK; ks += p.kps, ++it) {
-        const int s = static_cast<int>(it % S);
-        const uint32_t ph = (it / S) & 1u;
-        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, p.wait_limit_ns, p.status)) {
+      for (int ks = 0; ks < NK; ks += kps) {
+        const uint32_t s = rs, ph = rph;
+        if (++rs == S_) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
         }
-        for (int u = 0; u < p.kps; ++u) {
-          uint32_t w[4];
+        for (int u = 0; u < kps; ++u) {
+          // column j of the B scale block holds rows 32j + lane (j < 8: N <= 256)
+          uint32_t w[8];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 8; ++j) {
             const int r = 32 * j + lane;
-            w[j] = r < p.bn ? sfbt[r * stride + ks + u] : 0x7F7F7F7Fu;
+            w[j] = r < bn ? sfbt[r * stride + ks + u] : 0x7F7F7F7Fu;
           }
-          const uint32_t col = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 +
-                               (static_cast<uint32_t>(s) * static_cast<uint32_t>(p.kps) + u) * kSfColsPerChunk + 16u;
+          const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + u) * kSfColsPerChunk;
           __syncwarp();
-          tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
+          if (bn > 128) tmem_st_32x32b_x8(col, w);
+          else tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -454,14 +498,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(sh.sfbt_empty));
     }
-  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
     // ================================================================ epilogue
-    const int q = warp & 3;
-    uint32_t tcount = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+    const int q = warp & 3;                   // TMEM lane quarter of this warp
+    const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks
+    const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
+    uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
-      const uint32_t ab = tcount % static_cast<uint32_t>(p.acc_bufs);
-      const uint32_t aph = (tcount / static_cast<uint32_t>(p.acc_bufs)) & 1u;
+      ab = ab_next;
+      aph = aph_next;
+      if (++ab_next == acc_bufs) {
+        ab_next = 0;
+        aph_next ^= 1u;
+      }
       if (!warp_wait_bar(sh, &sh.acc_full[ab], aph, p.wait_limit_ns, p.status)) break;
       tc_fence_after();
       __syncwarp();
@@ -473,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int I32 = p.I / 32;
         // 16 columns at a time, each step over all 16 so that the per-column
         // chains (SwiGLU, warp amax, exponent, encode) overlap
-        for (int c0 = 0; c0 < tl.rows; c0 += 16) {
+        for (int c0 = 16 * half; c0 < tl.rows; c0 += 32) {
           uint32_t g[16], u[16];
           __syncwarp();
           tmem_ld_32x32b_x16(d0 + c0, g);
@@ -483,27 +533,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t amax[16];
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) {
+            // silu(g) * u with the fast reciprocal: h is re-quantised to 3
+            // mantissa bits right after, far coarser than its 2-ulp error
             const float gv = __uint_as_float(g[cc]);
-            h[cc] = gv / (1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
+            h[cc] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
             amax[cc] = __float_as_uint(h[cc]) & 0x7FFFFFFFu;
           }
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) amax[cc] = __reduce_max_sync(0xffffffffu, amax[cc]);
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
-            const int n = c0 + cc;
-            const int s = mx_block_exponent(amax[cc], 8);
-            const uint32_t code = enc_e4m3(h[cc] * pow2_neg(s));
-            if (n < tl.rows) {
-              const size_t row = static_cast<size_t>(tl.p0 + n);
-              p.h_codes[row * p.I + i] = static_cast<uint8_t>(code);
-              if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>(s + 127);
+          for (int cc = 0; cc < 16; cc += 2) {
+            const int s0 = mx_block_exponent(amax[cc], 8);
+            const int s1 = mx_block_exponent(amax[cc + 1], 8);
+            const uint32_t codes = enc_e4m3x2(h[cc] * pow2_neg(s0), h[cc + 1] * pow2_neg(s1));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const int n = c0 + cc + j;
+              if (n < tl.rows) {
+                const size_t row = static_cast<size_t>(tl.p0 + n);
+                p.h_codes[row * p.I + i] = static_cast<uint8_t>(codes >> (8 * j));
+                if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>((j ? s1 : s0) + 127);
+              }
             }
           }
         }
       } else {
         const bool two = 2 * tl.m + 1 < p.RB;
-        for (int c0 = 0; c0 < tl.rows; c0 += 32) {
+        for (int c0 = 32 * half; c0 < tl.rows; c0 += 64) {
           // lane n: token and combine weight of column c0 + n
           int tok = 0;
           float wt = 0.0f;
@@ -599,14 +655,6 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.RB = rows / 128;
   p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
   p.bn = a.bn;
-  p.kps = ((p.K / 128) % 2 == 0) ? 2 : 1;
-  if (const char* env = std::getenv("MXMOE_KPS")) {
-    const int v = std::atoi(env);
-    if (v == 1 || (v == 2 && (p.K / 128) % 2 == 0)) p.kps = v;
-  }
-  // two accumulator buffers (the epilogue of one tile overlaps the next tile's
-  // MMAs) whenever they leave tensor memory for two stages of scale factors
-  p.acc_bufs = (4u * static_cast<uint32_t>(a.bn) + 2u * kSfColsPerChunk * p.kps <= kTmemCols) ? 2 : 1;
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
   const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt);
@@ -621,30 +669,51 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
   p.sfbt_stride = p.NK + 1;
-  // Two 128-wide K chunks per pipeline stage (set above): the fixed per-stage
-  // costs of the single MMA-issuing thread (barrier waits, fences, scale
-  // copies, commit) are then paid once per 256 K.
   p.gather4 = a.gather4;
   p.pdl = a.pdl;
-  p.sf_col0 = 2u * static_cast<uint32_t>(p.acc_bufs) * static_cast<uint32_t>(p.bn);
 
-  // shared memory plan
+  // shared memory and tensor memory plan for `kps` 128-wide K chunks per
+  // pipeline stage: returns the stage count (0 if fewer than two fit)
   const uint32_t sfbt_bytes = (static_cast<uint32_t>(p.bn) * p.sfbt_stride * 4u + 1023u) & ~1023u;
   const uint32_t meta_bytes = (static_cast<uint32_t>(a.E + 2) * 8u + 127u) & ~127u;
-  const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u) * static_cast<uint32_t>(p.kps);
   int dev = 0;
   cudaGetDevice(&dev);
   int max_smem = 0;
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/;
-  int stages = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (const char* env = std::getenv("MXMOE_STAGES")) {  // tuning override (only lowers)
-    const int v = std::atoi(env);
-    if (v >= 2 && v < stages) stages = v;
+  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/ + 128u /*static*/;
+  const char* env_stages = std::getenv("MXMOE_STAGES");  // tuning override (only lowers)
+  auto plan = [&](int kps, int* acc_bufs, uint32_t* sf_col0) {
+    // two accumulator buffers (the epilogue of one tile overlaps the next
+    // tile's MMAs) whenever they leave tensor memory for two stages of scales
+    *acc_bufs = (4u * static_cast<uint32_t>(p.bn) + 2u * kSfColsPerChunk * kps <= kTmemCols) ? 2 : 1;
+    *sf_col0 = 2u * static_cast<uint32_t>(*acc_bufs) * static_cast<uint32_t>(p.bn);
+    if (*sf_col0 + 2u * kSfColsPerChunk * kps > kTmemCols) return 0;
+    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u) * static_cast<uint32_t>(kps);
+    if (static_cast<uint32_t>(max_smem) <= fixed) return 0;
+    int st = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
+    if (st > kMaxStages) st = kMaxStages;
+    if (env_stages) {
+      const int v = std::atoi(env_stages);
+      if (v >= 2 && v < st) st = v;
+    }
+    const int tmem_room = static_cast<int>((kTmemCols - *sf_col0) / (kSfColsPerChunk * kps));
+    if (st > tmem_room) st = tmem_room;
+    return st >= 2 ? st : 0;
+  };
+  // Two 128-wide K chunks per pipeline stage when two such stages fit: the
+  // fixed per-stage costs of the single MMA-issuing thread (barrier waits,
+  // fences, scale copies, commit) are then paid once per 256 K.
+  p.kps = 1;
+  if ((p.K / 128) % 2 == 0) {
+    int ab;
+    uint32_t sc;
+    if (plan(2, &ab, &sc) >= 2) p.kps = 2;
   }
-  const int tmem_room = static_cast<int>((kTmemCols - p.sf_col0) / (kSfColsPerChunk * p.kps));
-  if (stages > tmem_room) stages = tmem_room;
+  if (const char* env = std::getenv("MXMOE_KPS")) {
+    const int v = std::atoi(env);
+    if (v == 1 || (v == 2 && (p.K / 128) % 2 == 0)) p.kps = v;
+  }
+  const int stages = plan(p.kps, &p.acc_bufs, &p.sf_col0);
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
   uint32_t off = 0;

@@ -56,9 +56,8 @@ __device__ __forceinline__ void quantize_act_step(const uint4* __restrict__ x, i
   uint32_t packed[2] = {0u, 0u};
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const uint32_t c0 = enc_e4m3(__uint_as_float(w[m] << 16) * p);
-    const uint32_t c1 = enc_e4m3(__uint_as_float(w[m] & 0xFFFF0000u) * p);
-    packed[m >> 1] |= (c0 | (c1 << 8)) << ((m & 1) * 16);
+    const uint32_t c01 = enc_e4m3x2(__uint_as_float(w[m] << 16) * p, __uint_as_float(w[m] & 0xFFFF0000u) * p);
+    packed[m >> 1] |= c01 << ((m & 1) * 16);
   }
   if (valid) {
     codes[i] = make_uint2(packed[0], packed[1]);
@@ -110,7 +109,7 @@ __global__ void __launch_bounds__(256) k_quantize_weights(const float4* __restri
       if (fmt == MX_E4M3) {
         uint32_t packed = 0;
 #pragma unroll
-        for (int m = 0; m < 4; ++m) packed |= enc_e4m3(f[m] * p) << (8 * m);
+        for (int m = 0; m < 4; m += 2) packed |= enc_e4m3x2(f[m] * p, f[m + 1] * p) << (8 * m);
         reinterpret_cast<uint32_t*>(codes)[i] = packed;
       } else {
         uint32_t packed = 0;

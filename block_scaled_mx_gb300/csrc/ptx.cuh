@@ -148,7 +148,10 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
 // Same MMA with the two shared-memory descriptors given as their low 32-bit
 // halves and one shared high half (stride, version, swizzle): the issuing
 // thread then spends one add per operand per K step instead of rebuilding
-// 64-bit descriptors.
+// 64-bit descriptors.  No memory clobber: the MMA reads shared memory
+// asynchronously, ordered by mbarriers and tcgen05 fences, not by the
+// compiler, and a clobber would make the issuing thread reload values between
+// MMAs (the thread's instruction count per MMA sets the issue rate).
 __device__ __forceinline__ void mma_mxf8f6f4_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
                                                 uint32_t desc_hi, uint32_t idesc, uint32_t sfa_tmem,
                                                 uint32_t sfb_tmem, uint32_t accumulate) {
@@ -158,8 +161,7 @@ __device__ __forceinline__ void mma_mxf8f6f4_lo(uint32_t d_tmem, uint32_t a_lo, 
       "mov.b64 ad, {%1, %7};\n\t"
       "mov.b64 bd, {%2, %7};\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], ad, bd, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem), "r"(desc_hi)
-      : "memory");
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem), "r"(desc_hi));
 }
 // Low / high halves of the K-major, 128-byte-swizzled operand descriptor with
 // 8-row groups 1024 bytes apart (see smem_desc).
@@ -177,13 +179,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // Shared -> tensor memory: 32 rows x 128 bit, replicated into all four lane
 // quarters (lane l of every quarter receives row l).
 __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
 }
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, uint32_t r1,
                                                   uint32_t r2, uint32_t r3) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r0),
                "r"(r1), "r"(r2), "r"(r3)
                : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

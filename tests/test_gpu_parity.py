@@ -297,3 +297,19 @@ def test_layer_parity_other_stage_shape(name, kps, monkeypatch):
     assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
     rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
     assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+
+
+@pytest.mark.parametrize("name,bn", [("wide_e4m3", "96"), ("wide_e4m3", "224"), ("wide_e2m1", "128"),
+                                     ("wide_e2m1", "160"), ("decode_mxfp8", "64"), ("ragged_e4m3", "192")])
+def test_layer_parity_other_tile_width(name, bn, monkeypatch):
+    """Other token-tile widths than the shape's default: two accumulator buffers
+    (96), one buffer with one or two K chunks per stage (128 .. 224), the gather4
+    schedule at 64 rows, and a wide tile on a shape whose experts hold few rows."""
+    monkeypatch.setenv("MXMOE_BN", bn)
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle_forward(L)
+    out = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
