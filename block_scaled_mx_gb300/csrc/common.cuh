@@ -9,20 +9,14 @@
 
 namespace mxk {
 
-// floor(log2(a)) for a finite a > 0 given its fp32 bit pattern (sign cleared);
-// fp32 subnormals are m * 2^-149.
-__device__ __forceinline__ int floor_log2_bits(uint32_t a) {
-  const int ef = static_cast<int>(a >> 23);
-  if (ef > 0) return ef - 127;
-  return -149 + (31 - __clz(a & 0x7FFFFFu));
-}
-
-// Shared block exponent s = clamp(floor(log2(amax)) - emax, -127, 127); an
-// all-zero block (amax = 0, log2 = -inf) takes the lower clamp.
+// Shared block exponent s = clamp(floor(log2(amax)) - emax, -127, 127) for a
+// finite amax given as fp32 bits with the sign cleared, emax >= 0.  Written
+// without branches: a normal amax has floor(log2) = biased exponent - 127; a
+// subnormal or zero amax (biased exponent 0, log2 below -126, or -inf for 0)
+// always lands at the lower clamp, and so does the formula with exponent 0;
+// the upper clamp is never reached (biased exponent <= 254, emax >= 0).
 __device__ __forceinline__ int mx_block_exponent(uint32_t amax_bits, int emax) {
-  if (amax_bits == 0u) return -127;
-  int s = floor_log2_bits(amax_bits) - emax;
-  return s < -127 ? -127 : (s > 127 ? 127 : s);
+  return max(static_cast<int>(amax_bits >> 23) - 127 - emax, -127);
 }
 
 // 2^-s as an fp32 for s in [-127, 126] (exact power of two).

@@ -46,6 +46,7 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpSf0 = 4;
 constexpr int kWarpEpi0 = 8;
 constexpr int kEpiWarps = 8;
+constexpr uint32_t kEpiBufBytes = 2048;  // per epilogue warp: a 16-column transpose tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
 constexpr int kMaxStages = 8;
@@ -66,7 +67,7 @@ struct GemmParams {
   float* out;
   int* status;
   unsigned long long wait_limit_ns;
-  uint32_t off_a, off_b, off_sfa, off_sfbt, off_meta, off_bar;
+  uint32_t off_a, off_b, off_sfa, off_sfbt, off_meta, off_bar, off_epi;
   uint32_t sf_col0;
   int sfbt_stride;  // words per row of the per-tile B scale table (NK + 1)
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
@@ -120,7 +121,7 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(b, parity)) return true;
+    if (mbar_try_wait_sleep(b, parity, 20000u)) return true;
     if (*sh.abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       set_status(status, MX_ERR_TIMEOUT);
@@ -502,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ epilogue
     const int q = warp & 3;                   // TMEM lane quarter of this warp
     const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks
+    uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * kEpiBufBytes;
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -519,8 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t d0 = tbase + lane_base + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
       const uint32_t d1 = tbase + lane_base + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
       if (p.epi == 0) {
-        const int i = tl.m * 128 + 32 * q + lane;
-        const int I32 = p.I / 32;
+        const int i0 = tl.m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
+        const int I = p.I, I32 = p.I / 32;
+        uint8_t* const h_codes = p.h_codes;
+        uint8_t* const h_scales = p.h_scales;
         // 16 columns at a time, each step over all 16 so that the per-column
         // chains (SwiGLU, warp amax, exponent, encode) overlap
         for (int c0 = 16 * half; c0 < tl.rows; c0 += 32) {
@@ -541,24 +545,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) amax[cc] = __reduce_max_sync(0xffffffffu, amax[cc]);
+          // codes go through a per-warp shared-memory tile [16 columns][32 rows
+          // of I] so that each lane writes one 16-byte run of an h row (byte
+          // stores from every lane, one per column, throttle the store path)
+          int my_s = 0;  // lane j < 16: the scale of column j
 #pragma unroll
           for (int cc = 0; cc < 16; cc += 2) {
             const int s0 = mx_block_exponent(amax[cc], 8);
             const int s1 = mx_block_exponent(amax[cc + 1], 8);
             const uint32_t codes = enc_e4m3x2(h[cc] * pow2_neg(s0), h[cc + 1] * pow2_neg(s1));
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-              const int n = c0 + cc + j;
-              if (n < tl.rows) {
-                const size_t row = static_cast<size_t>(tl.p0 + n);
-                p.h_codes[row * p.I + i] = static_cast<uint8_t>(codes >> (8 * j));
-                if (lane == 0) p.h_scales[row * I32 + i / 32] = static_cast<uint8_t>((j ? s1 : s0) + 127);
-              }
-            }
+            ebuf[cc * 32 + lane] = static_cast<uint8_t>(codes);
+            ebuf[(cc + 1) * 32 + lane] = static_cast<uint8_t>(codes >> 8);
+            if (lane == cc) my_s = s0;
+            if (lane == cc + 1) my_s = s1;
           }
+          __syncwarp();
+          const int nvalid = tl.rows - c0;
+          const int col = lane >> 1;
+          const uint4 v = *reinterpret_cast<const uint4*>(ebuf + col * 32 + (lane & 1) * 16);
+          if (col < nvalid)
+            *reinterpret_cast<uint4*>(h_codes + static_cast<size_t>(tl.p0 + c0 + col) * I + i0 + (lane & 1) * 16) = v;
+          if (lane < 16 && lane < nvalid)
+            h_scales[static_cast<size_t>(tl.p0 + c0 + lane) * I32 + i0 / 32] = static_cast<uint8_t>(my_s + 127);
+          __syncwarp();
         }
       } else {
         const bool two = 2 * tl.m + 1 < p.RB;
+        float* const out = p.out;
+        const int H = p.H;
+        float* const ebf = reinterpret_cast<float*>(ebuf);
         for (int c0 = 32 * half; c0 < tl.rows; c0 += 64) {
           // lane n: token and combine weight of column c0 + n
           int tok = 0;
@@ -575,20 +590,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int sub = 0; sub < (two ? 2 : 1); ++sub) {
             const uint32_t d = sub == 0 ? d0 : d1;
-            const int o = tl.m * 256 + sub * 128 + 32 * q + lane;
+            const int o0 = tl.m * 256 + sub * 128 + 32 * q;  // this warp's 32 rows of H
             for (int h0 = 0; h0 < 32 && c0 + h0 < tl.rows; h0 += 16) {
               uint32_t a[16];
               __syncwarp();
               tmem_ld_32x32b_x16(d + c0 + h0, a);
               tmem_ld_wait();
+              // weighted values through the per-warp transpose tile [16 columns]
+              // [32 rows of H], then four consecutive H values per lane and
+              // column: one 16-byte vector reduction instead of four scalar ones
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc) {
-                const int n = h0 + cc;
-                const int tn = __shfl_sync(0xffffffffu, tok, n);
-                const float wn = __shfl_sync(0xffffffffu, wt, n);
-                if (c0 + n < tl.rows && wn != 0.0f)
-                  atomicAdd(p.out + static_cast<size_t>(tn) * p.H + o, wn * __uint_as_float(a[cc]));
+              for (int cc = 0; cc < 16; ++cc)
+                ebf[cc * 32 + lane] = __shfl_sync(0xffffffffu, wt, h0 + cc) * __uint_as_float(a[cc]);
+              __syncwarp();
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const int col = 4 * r + (lane >> 3);
+                const int tn = __shfl_sync(0xffffffffu, tok, h0 + col);
+                const float4 v = *reinterpret_cast<const float4*>(ebf + col * 32 + (lane & 7) * 4);
+                if (c0 + h0 + col < tl.rows) red_add_v4(out + static_cast<size_t>(tn) * H + o0 + (lane & 7) * 4, v);
               }
+              __syncwarp();
             }
           }
         }
@@ -680,7 +702,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   int max_smem = 0;
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/ + 128u /*static*/;
+  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/ + 128u /*static*/ +
+                         kEpiWarps * kEpiBufBytes;
   const char* env_stages = std::getenv("MXMOE_STAGES");  // tuning override (only lowers)
   auto plan = [&](int kps, int* acc_bufs, uint32_t* sf_col0) {
     // two accumulator buffers (the epilogue of one tile overlaps the next
@@ -729,6 +752,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   off += meta_bytes;
   p.off_bar = off;
   off += 512u;
+  p.off_epi = off;
+  off += kEpiWarps * kEpiBufBytes;
   const size_t smem = static_cast<size_t>(off) + 1024u;
 
   // tensor maps
