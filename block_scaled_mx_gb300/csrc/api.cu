@@ -230,8 +230,8 @@ int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* counts, i
 size_t moe_prepared_weight_bytes(int E1, int H, int I, int fmt, int which) {
   if (E1 <= 0 || H <= 0 || I <= 0 || (fmt != MX_E4M3 && fmt != MX_E2M1)) return 0;
   if (H % 128 || I % 128) return 0;
-  if (which == 1) return prepared_layout(E1, 2 * I, H, fmt).total_bytes;
-  if (which == 2) return prepared_layout(E1, H, I, fmt).total_bytes;
+  if (which == 1) return prepared_layout(E1, 2 * I, H, fmt, 1).total_bytes;
+  if (which == 2) return prepared_layout(E1, H, I, fmt, 0).total_bytes;
   return 0;
 }
 
@@ -242,7 +242,8 @@ int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int
   if (!codes || !scales || !dst) return MX_ERR_INVALID_ARG;
   if (H % 128 || I % 128) return MX_ERR_UNSUPPORTED;
   if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(dst, 256)) return MX_ERR_ALIGNMENT;
-  const PreparedLayout L = which == 1 ? prepared_layout(E1, 2 * I, H, fmt) : prepared_layout(E1, H, I, fmt);
+  const PreparedLayout L =
+      which == 1 ? prepared_layout(E1, 2 * I, H, fmt, 1) : prepared_layout(E1, H, I, fmt, 0);
   if (dst_bytes < L.total_bytes) return MX_ERR_WORKSPACE;
   return cuda_status(launch_prepare_weights(codes, scales, L, static_cast<uint8_t*>(dst),
                                             reinterpret_cast<cudaStream_t>(stream)));

@@ -246,17 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
-      int rb0, rb1;
-      bool two;
-      if (p.epi == 0) {
-        rb0 = tl.m;
-        rb1 = p.RB / 2 + tl.m;
-        two = true;
-      } else {
-        rb0 = 2 * tl.m;
-        rb1 = 2 * tl.m + 1;
-        two = rb1 < p.RB;
-      }
+      // the tile's two row blocks are prepared blocks 2m and 2m + 1 of each K
+      // chunk (gate and up block m in W1): one TMA box and one scale bulk copy
+      const bool two = 2 * tl.m + 1 < p.RB;
       // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token)
       const int n4 = gather ? (tl.rows + 3) / 4 : 0;
       int tok[4] = {0, 0, 0, 0};
@@ -270,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
-      const uint32_t bytes = ((p.a_tx + 512u) * (two ? 2u : 1u) + b_bytes) * static_cast<uint32_t>(kps);
+      const uint32_t sfa_bytes = two ? 1024u : 512u;
+      const uint32_t bytes = (2u * p.a_tx + sfa_bytes + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
@@ -285,14 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kc = ks + u;
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
             uint8_t* sfa_s = base + p.off_sfa + (su + u) * 1024u;
-            const int blk0 = (tl.e * p.RB + rb0) * NK + kc;
+            // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
+            // the TMA fills zeros and still counts the whole box)
+            const int blk0 = (tl.e * NK + kc) * p.RB + 2 * tl.m;
             tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
-            bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, 512u, full);
-            if (two) {
-              const int blk1 = (tl.e * p.RB + rb1) * NK + kc;
-              tma_load_3d(smem_u32(a_s + 16384), &tm_a, 0, 0, blk1, full);
-              bulk_load(smem_u32(sfa_s + 512), p.w_scales + static_cast<size_t>(blk1) * 512u, 512u, full);
-            }
+            bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, sfa_bytes, full);
           }
         }
         if (!b_ready) {
@@ -679,7 +669,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.bn = a.bn;
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
-  const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt);
+  const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt, a.epi == 0 ? 1 : 0);
   p.w_scales = static_cast<const uint8_t*>(a.w_prep) + L.scales_offset;
   p.b_scales = a.b_scales;
   p.offsets = a.offsets;
@@ -762,7 +752,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   {
     cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(nblk)};
     cuuint64_t strides[2];
-    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t box[3] = {128, 128, 2};  // two row blocks per box
     cuuint32_t es[3] = {1, 1, 1};
     CUtensorMapDataType dt;
     if (a.fmt == MX_E4M3) {

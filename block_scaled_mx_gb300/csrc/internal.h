@@ -65,10 +65,11 @@ cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
 struct PreparedLayout {
   int E1, rows, K, fmt;
   int RB, NK;
+  int interleave;           // W1: prepared row block 2m is gate block m, 2m + 1 is up block m
   size_t block_code_bytes;  // 16384 (E4M3) or 8192 (E2M1)
   size_t codes_bytes, scales_offset, scales_bytes, total_bytes;
 };
-PreparedLayout prepared_layout(int E1, int rows, int K, int fmt);
+PreparedLayout prepared_layout(int E1, int rows, int K, int fmt, int interleave);
 cudaError_t launch_prepare_weights(const uint8_t* codes, const uint8_t* scales,
                                    const PreparedLayout& L, uint8_t* dst, cudaStream_t s);
 

@@ -489,7 +489,12 @@ cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
 }
 
 // ------------------------------------------------------------------ weight re-layout
-PreparedLayout prepared_layout(int E1, int rows, int K, int fmt) {
+// Block (e, kc, rb') of 128 rows x 128 K elements sits at linear index
+// (e * NK + kc) * RB + rb': for one K chunk, all row blocks of an expert are
+// adjacent, so the two row blocks a GEMM tile multiplies (gate block m and up
+// block m, interleaved as rb' = 2m and 2m + 1 in W1; row blocks 2m and 2m + 1 in
+// W2) arrive with one TMA box and their scale blocks with one bulk copy.
+PreparedLayout prepared_layout(int E1, int rows, int K, int fmt, int interleave) {
   PreparedLayout L;
   L.E1 = E1;
   L.rows = rows;
@@ -497,6 +502,7 @@ PreparedLayout prepared_layout(int E1, int rows, int K, int fmt) {
   L.fmt = fmt;
   L.RB = rows / 128;
   L.NK = K / 128;
+  L.interleave = interleave;
   L.block_code_bytes = fmt == MX_E4M3 ? 16384 : 8192;
   const size_t nblk = static_cast<size_t>(E1) * L.RB * L.NK;
   L.codes_bytes = nblk * L.block_code_bytes;
@@ -506,9 +512,14 @@ PreparedLayout prepared_layout(int E1, int rows, int K, int fmt) {
   return L;
 }
 
+// canonical row block of prepared row block rb'
+__device__ __forceinline__ int canonical_rb(int rbp, int RB, int interleave) {
+  return interleave ? ((rbp & 1) ? RB / 2 + (rbp >> 1) : (rbp >> 1)) : rbp;
+}
+
 // codes: one thread per 16-byte chunk of the destination block
 __global__ void __launch_bounds__(256) k_prepare_codes(const uint4* __restrict__ src, int rows,
-                                                       int64_t src_row_chunks, int RB, int NK,
+                                                       int64_t src_row_chunks, int RB, int NK, int interleave,
                                                        int blk_row_chunks, int64_t total,
                                                        uint4* __restrict__ dst) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -518,10 +529,11 @@ __global__ void __launch_bounds__(256) k_prepare_codes(const uint4* __restrict__
     const int64_t b = i / per_blk;
     const int within = static_cast<int>(i - b * per_blk);
     const int r = within / blk_row_chunks, c = within - r * blk_row_chunks;
-    const int kc = static_cast<int>(b % NK);
-    const int64_t erb = b / NK;
-    const int rb = static_cast<int>(erb % RB);
-    const int64_t e = erb / RB;
+    const int rbp = static_cast<int>(b % RB);
+    const int64_t ekc = b / RB;
+    const int kc = static_cast<int>(ekc % NK);
+    const int64_t e = ekc / NK;
+    const int rb = canonical_rb(rbp, RB, interleave);
     const int64_t src_row = e * rows + static_cast<int64_t>(rb) * 128 + r;
     dst[i] = __ldg(&src[src_row * src_row_chunks + static_cast<int64_t>(kc) * blk_row_chunks + c]);
   }
@@ -531,18 +543,19 @@ __global__ void __launch_bounds__(256) k_prepare_codes(const uint4* __restrict__
 // the four k-blocks of row 32*j + l (the tensor-memory scale-factor layout of
 // the block-scaled MMA, copied in by tcgen05.cp 32x128b.warpx4).
 __global__ void __launch_bounds__(256) k_prepare_scales(const uint8_t* __restrict__ src, int rows,
-                                                        int K32, int RB, int NK, int64_t total_words,
-                                                        uint32_t* __restrict__ dst) {
+                                                        int K32, int RB, int NK, int interleave,
+                                                        int64_t total_words, uint32_t* __restrict__ dst) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_words;
        i += stride) {
     const int64_t b = i / 128;
     const int w = static_cast<int>(i & 127);
     const int l = w >> 2, j = w & 3;
-    const int kc = static_cast<int>(b % NK);
-    const int64_t erb = b / NK;
-    const int rb = static_cast<int>(erb % RB);
-    const int64_t e = erb / RB;
+    const int rbp = static_cast<int>(b % RB);
+    const int64_t ekc = b / RB;
+    const int kc = static_cast<int>(ekc % NK);
+    const int64_t e = ekc / NK;
+    const int rb = canonical_rb(rbp, RB, interleave);
     const int64_t row = e * rows + static_cast<int64_t>(rb) * 128 + 32 * j + l;
     dst[i] = __ldg(reinterpret_cast<const uint32_t*>(src + row * K32 + static_cast<int64_t>(kc) * 4));
   }
@@ -556,13 +569,13 @@ cudaError_t launch_prepare_weights(const uint8_t* codes, const uint8_t* scales,
   const int64_t total = nblk * 128 * blk_row_chunks;
   if (total > 0) {
     k_prepare_codes<<<grid_for(total, 256, 8), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(codes), L.rows, src_row_chunks, L.RB, L.NK, blk_row_chunks,
-        total, reinterpret_cast<uint4*>(dst));
+        reinterpret_cast<const uint4*>(codes), L.rows, src_row_chunks, L.RB, L.NK, L.interleave,
+        blk_row_chunks, total, reinterpret_cast<uint4*>(dst));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t words = nblk * 128;
     k_prepare_scales<<<grid_for(words, 256, 8), 256, 0, s>>>(
-        scales, L.rows, L.K / 32, L.RB, L.NK, words,
+        scales, L.rows, L.K / 32, L.RB, L.NK, L.interleave, words,
         reinterpret_cast<uint32_t*>(dst + L.scales_offset));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
