@@ -32,7 +32,7 @@ int choose_bn(int T, int E, int k, int which) {
   const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
   if (env) {
     const int v = std::atoi(env);
-    if (v >= 32 && v <= 224 && v % 32 == 0) return v;
+    if (v >= 32 && v <= 224 && v % 16 == 0) return v;
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
   if (mean_rows < 48.0) return 32;

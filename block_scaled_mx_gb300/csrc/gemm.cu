@@ -46,7 +46,9 @@ constexpr int kWarpMma = 1;
 constexpr int kWarpSf0 = 4;
 constexpr int kWarpEpi0 = 8;
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kEpiBufBytes = 2048;  // per epilogue warp: a 16-column transpose tile
+// per epilogue warp, a transpose tile: 16 columns of E4M3 codes (gate/up) or
+// 8 columns of fp32 (down)
+__host__ __device__ constexpr uint32_t epi_buf_bytes(int epi) { return epi == 0 ? 512u : 1024u; }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
 constexpr int kMaxStages = 8;
@@ -67,9 +69,8 @@ struct GemmParams {
   float* out;
   int* status;
   unsigned long long wait_limit_ns;
-  uint32_t off_a, off_b, off_sfa, off_sfbt, off_meta, off_bar, off_epi;
+  uint32_t off_a, off_b, off_sfa, off_meta, off_bar, off_epi;
   uint32_t sf_col0;
-  int sfbt_stride;  // words per row of the per-tile B scale table (NK + 1)
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
   int pdl;          // see GemmArgs::pdl
   int kps;          // 128-wide K chunks per pipeline stage (1 or 2)
@@ -90,8 +91,6 @@ struct Shared {
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
-  uint64_t* sfbt_full;   // per-tile B scale table loaded (128 arrivals)
-  uint64_t* sfbt_empty;  // per-tile B scale table consumed (4 arrivals)
   uint32_t* tmem_slot;
 };
 
@@ -159,10 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.acc_full = bars + 3 * S;
   sh.acc_empty = bars + 3 * S + 2;
   sh.drain = bars + 3 * S + 4;
-  sh.sfbt_full = bars + 3 * S + 5;
-  sh.sfbt_empty = bars + 3 * S + 6;
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 7);
-  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S + 8);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S + 6);
 
   // ---- prologue: expert offsets, per-expert tile counts and their prefix
   const int E1 = p.E + 1;
@@ -180,8 +177,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sh.acc_empty[a]), kEpiWarps);
     }
     mbar_init(smem_u32(sh.drain), 1);
-    mbar_init(smem_u32(sh.sfbt_full), 128);
-    mbar_init(smem_u32(sh.sfbt_empty), 4);
     *sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -402,98 +397,77 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
     // ================================================================ B scale staging
+    // Per stage, the token-row scales of its K chunks are read from global
+    // memory (one 32-bit word per row and chunk; L2-resident, and issued before
+    // the slot is free so their latency overlaps the wait) and stored with
+    // tcgen05.st into this warp's TMEM lane quarter (all four quarters hold the
+    // same words).
     const int q = warp & 3;
-    const int sft = tid - kWarpSf0 * 32;
-    uint32_t* sfbt = reinterpret_cast<uint32_t*>(base + p.off_sfbt);
-    const int stride = p.sfbt_stride;
     const int K32 = p.K / 32;
     const uint32_t S_ = static_cast<uint32_t>(S);
     const int kps = p.kps, bn = p.bn;
     const unsigned long long lim = p.wait_limit_ns;
     int* const status = p.status;
     const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 + 16u;
-    uint32_t rs = 0, rph = 0, tj = 0;
+    uint32_t rs = 0, rph = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tj) {
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
-      // the previous tile's table has been consumed by all four warps
-      if (!warp_wait_bar(sh, sh.sfbt_empty, (tj & 1u) ^ 1u, p.wait_limit_ns, p.status)) break;
-      // one row per thread: its token is looked up once, then the row's NK scale
-      // words are fetched with independent 16-byte loads (a loop of dependent
-      // slot -> token -> scale loads here cost tens of microseconds per tile)
-      for (int r = sft; r < p.bn; r += 128) {
-        if (r >= tl.rows) {
-          for (int c = 0; c < NK; ++c) sfbt[r * stride + c] = 0x7F7F7F7Fu;
-          continue;
-        }
-        int src_row = tl.p0 + r;
-        if (p.epi == 0) {
-          src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
-          if (src_row < 0 || src_row >= p.T) {
-            set_status(p.status, MX_ERR_DEVICE_ARG);
-            src_row = 0;
-          }
-        }
-        const uint8_t* srow = p.b_scales + static_cast<size_t>(src_row) * K32;
-        if ((NK & 3) == 0) {
-          uint4 v[8];
-          for (int c0 = 0; c0 < NK; c0 += 32) {
+      // rows 32j + lane of this tile: their scale rows (null: a padding row)
+      const uint32_t* rowp[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              if (c0 + 4 * u < NK) v[u] = __ldg(reinterpret_cast<const uint4*>(srow) + (c0 / 4 + u));
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              if (c0 + 4 * u < NK) {
-                uint32_t* d = sfbt + r * stride + c0 + 4 * u;
-                d[0] = v[u].x;
-                d[1] = v[u].y;
-                d[2] = v[u].z;
-                d[3] = v[u].w;
-              }
+      for (int j = 0; j < 8; ++j) {
+        const int r = 32 * j + lane;
+        rowp[j] = nullptr;
+        if (r < tl.rows) {
+          int src_row = tl.p0 + r;
+          if (p.epi == 0) {
+            src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
+            if (src_row < 0 || src_row >= p.T) {
+              set_status(status, MX_ERR_DEVICE_ARG);
+              src_row = 0;
+            }
           }
-        } else {
-          for (int c = 0; c < NK; ++c) sfbt[r * stride + c] = __ldg(reinterpret_cast<const uint32_t*>(srow) + c);
+          rowp[j] = reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32);
         }
       }
-      mbar_arrive(smem_u32(sh.sfbt_full));
-      if (!warp_wait_bar(sh, sh.sfbt_full, tj & 1u, p.wait_limit_ns, p.status)) break;
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (++rs == S_) {
           rs = 0;
           rph ^= 1u;
         }
+        uint32_t bw[2][8];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) bw[u][j] = (u < kps && rowp[j]) ? __ldg(rowp[j] + ks + u) : 0x7F7F7F7Fu;
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
         }
-        for (int u = 0; u < kps; ++u) {
-          // column j of the B scale block holds rows 32j + lane (j < 8: N <= 256)
-          uint32_t w[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int r = 32 * j + lane;
-            w[j] = r < bn ? sfbt[r * stride + ks + u] : 0x7F7F7F7Fu;
+        for (int u = 0; u < 2; ++u) {
+          if (u < kps) {
+            // column j of the B scale block holds rows 32j + lane (j < 8: N <= 256)
+            const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + u) * kSfColsPerChunk;
+            __syncwarp();
+            if (bn > 128) tmem_st_32x32b_x8(col, bw[u]);
+            else tmem_st_32x32b_x4(col, bw[u][0], bw[u][1], bw[u][2], bw[u][3]);
           }
-          const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + u) * kSfColsPerChunk;
-          __syncwarp();
-          if (bn > 128) tmem_st_32x32b_x8(col, w);
-          else tmem_st_32x32b_x4(col, w[0], w[1], w[2], w[3]);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.sfb_ready[s]));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(sh.sfbt_empty));
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
     // ================================================================ epilogue
     const int q = warp & 3;                   // TMEM lane quarter of this warp
     const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks
-    uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * kEpiBufBytes;
+    uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(p.epi);
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -586,21 +560,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
               tmem_ld_32x32b_x16(d + c0 + h0, a);
               tmem_ld_wait();
-              // weighted values through the per-warp transpose tile [16 columns]
+              // weighted values through the per-warp transpose tile [8 columns]
               // [32 rows of H], then four consecutive H values per lane and
               // column: one 16-byte vector reduction instead of four scalar ones
 #pragma unroll
-              for (int cc = 0; cc < 16; ++cc)
-                ebf[cc * 32 + lane] = __shfl_sync(0xffffffffu, wt, h0 + cc) * __uint_as_float(a[cc]);
-              __syncwarp();
+              for (int c8 = 0; c8 < 16; c8 += 8) {
 #pragma unroll
-              for (int r = 0; r < 4; ++r) {
-                const int col = 4 * r + (lane >> 3);
-                const int tn = __shfl_sync(0xffffffffu, tok, h0 + col);
-                const float4 v = *reinterpret_cast<const float4*>(ebf + col * 32 + (lane & 7) * 4);
-                if (c0 + h0 + col < tl.rows) red_add_v4(out + static_cast<size_t>(tn) * H + o0 + (lane & 7) * 4, v);
+                for (int cc = 0; cc < 8; ++cc)
+                  ebf[cc * 32 + lane] = __shfl_sync(0xffffffffu, wt, h0 + c8 + cc) * __uint_as_float(a[c8 + cc]);
+                __syncwarp();
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                  const int col = c8 + 4 * r + (lane >> 3);
+                  const int tn = __shfl_sync(0xffffffffu, tok, h0 + col);
+                  const float4 v = *reinterpret_cast<const float4*>(ebf + (col - c8) * 32 + (lane & 7) * 4);
+                  if (c0 + h0 + col < tl.rows)
+                    red_add_v4(out + static_cast<size_t>(tn) * H + o0 + (lane & 7) * 4, v);
+                }
+                __syncwarp();
               }
-              __syncwarp();
             }
           }
         }
@@ -680,20 +658,18 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.out = a.out;
   p.status = a.status;
   p.wait_limit_ns = a.wait_limit_ns;
-  p.sfbt_stride = p.NK + 1;
   p.gather4 = a.gather4;
   p.pdl = a.pdl;
 
   // shared memory and tensor memory plan for `kps` 128-wide K chunks per
   // pipeline stage: returns the stage count (0 if fewer than two fit)
-  const uint32_t sfbt_bytes = (static_cast<uint32_t>(p.bn) * p.sfbt_stride * 4u + 1023u) & ~1023u;
   const uint32_t meta_bytes = (static_cast<uint32_t>(a.E + 2) * 8u + 127u) & ~127u;
   int dev = 0;
   cudaGetDevice(&dev);
   int max_smem = 0;
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const uint32_t fixed = 1024u /*align slack*/ + sfbt_bytes + meta_bytes + 512u /*barriers*/ + 128u /*static*/ +
-                         kEpiWarps * kEpiBufBytes;
+  const uint32_t epi_bytes = kEpiWarps * epi_buf_bytes(a.epi);
+  const uint32_t fixed = 1024u /*align slack*/ + meta_bytes + 512u /*barriers*/ + 128u /*static*/ + epi_bytes;
   const char* env_stages = std::getenv("MXMOE_STAGES");  // tuning override (only lowers)
   auto plan = [&](int kps, int* acc_bufs, uint32_t* sf_col0) {
     // two accumulator buffers (the epilogue of one tile overlaps the next
@@ -722,7 +698,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     uint32_t sc;
     if (plan(2, &ab, &sc) >= 2) p.kps = 2;
   }
-  if (const char* env = std::getenv("MXMOE_KPS")) {
+  if (const char* env = std::getenv(a.epi == 1 && std::getenv("MXMOE_KPS2") ? "MXMOE_KPS2" : "MXMOE_KPS")) {
     const int v = std::atoi(env);
     if (v == 1 || (v == 2 && (p.K / 128) % 2 == 0)) p.kps = v;
   }
@@ -736,14 +712,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   off += static_cast<uint32_t>(stages * p.kps) * p.bn * 128u;
   p.off_sfa = off;
   off += static_cast<uint32_t>(stages * p.kps) * 1024u;
-  p.off_sfbt = off;
-  off += sfbt_bytes;
   p.off_meta = off;
   off += meta_bytes;
   p.off_bar = off;
   off += 512u;
   p.off_epi = off;
-  off += kEpiWarps * kEpiBufBytes;
+  off += epi_bytes;
   const size_t smem = static_cast<size_t>(off) + 1024u;
 
   // tensor maps
