@@ -22,12 +22,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 // Token-row tile width of the grouped GEMMs, chosen from the mean rows per
 // expert (known on the host, no device read).  The narrow decode schedule
 // (32 rows) streams weights with two accumulator buffers.  The wide prefill
-// schedule reuses each weight tile over many token rows: 192 for the gate/up
-// GEMM (one accumulator buffer: a block-scaled MMA costs about the same issue
-// time for any N up to 192, so doubling N over 96 outweighs the epilogue no
-// longer overlapping the MMAs) and 96 for the down GEMM, whose atomic combine
-// epilogue is too long to leave un-overlapped (two buffers).
-// `which`: 0 gate/up, 1 down.
+// schedule reuses each weight tile over 192 token rows with one accumulator
+// buffer: a block-scaled MMA costs about the same issue time for any N up to
+// 192, so doubling N over 96 (the widest tile with two buffers) outweighs the
+// epilogue no longer overlapping the MMAs.  `which`: 0 gate/up, 1 down.
 int choose_bn(int T, int E, int k, int which) {
   const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
   if (env) {
@@ -36,7 +34,7 @@ int choose_bn(int T, int E, int k, int which) {
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
   if (mean_rows < 48.0) return 32;
-  return which == 0 ? 192 : 96;
+  return 192;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {

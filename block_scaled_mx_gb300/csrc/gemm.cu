@@ -56,6 +56,9 @@ constexpr int kMaxStages = 8;
 struct GemmParams {
   int epi, afmt, T, H, I, E, k;
   int K, NK, NM, RB;
+  int MG;  // weight tiles per tile group: groups of MG weight tiles (of every expert and
+           // token tile) run one after the other, so the down GEMM's combine targets
+           // one slice of `out` at a time (L2-resident atomics)
   int bn, stages, acc_bufs;
   int n_rows;
   uint32_t a_tx;
@@ -94,7 +97,12 @@ struct Shared {
   uint32_t* tmem_slot;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int NM, int bn) {
+// Tile t -> (group, expert, token tile, weight tile).  Tiles are ordered group-
+// major, then expert, token tile and weight tile within the group; prefix[e]
+// counts one group's tiles of the experts before e.
+__device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int MG, int bn, int per_group) {
+  const int g = t / per_group;
+  t -= g * per_group;
   int lo = 0, hi = E;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -104,8 +112,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int 
   Tile tl;
   tl.e = lo;
   const int local = t - sh.prefix[lo];
-  const int nt = local / NM;
-  tl.m = local - nt * NM;
+  const int nt = local / MG;
+  tl.m = g * MG + (local - nt * MG);
   const int cnt = sh.offs[lo + 1] - sh.offs[lo];
   const int n0 = nt * bn;
   tl.rows = min(bn, cnt - n0);
@@ -193,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int run = 0;
     for (int e = b0; e < b1; ++e) {
       const int cnt = sh.offs[e + 1] - sh.offs[e];
-      run += p.NM * ((cnt + p.bn - 1) / p.bn);
+      run += p.MG * ((cnt + p.bn - 1) / p.bn);
     }
     int incl = run;
 #pragma unroll
@@ -208,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = b0; e < b1; ++e) {
       sh.prefix[e] = acc;
       const int cnt = sh.offs[e + 1] - sh.offs[e];
-      acc += p.NM * ((cnt + p.bn - 1) / p.bn);
+      acc += p.MG * ((cnt + p.bn - 1) / p.bn);
     }
     if (b1 == E1 && b0 < b1) sh.prefix[E1] = acc;
     if (E1 == 0 && tid == 0) sh.prefix[0] = 0;
@@ -217,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *sh.tmem_slot;
-  const int total = sh.prefix[E1];
+  const int per_group = sh.prefix[E1];
+  const int total = per_group * (p.NM / p.MG);
   const int NK = p.NK;
 
   if (warp == kWarpTma) {
@@ -240,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
       // the tile's two row blocks are prepared blocks 2m and 2m + 1 of each K
       // chunk (gate and up block m in W1): one TMA box and one scale bulk copy
       const bool two = 2 * tl.m + 1 < p.RB;
@@ -333,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_lo0 = desc_lo_sw128(b_base);
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+        const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
         const bool two = p.epi == 0 || (2 * tl.m + 1 < p.RB);
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
@@ -413,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
       // rows 32j + lane of this tile: their scale rows (null: a padding row)
       const uint32_t* rowp[8];
 #pragma unroll
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile(t, sh, p.E, p.NM, p.bn);
+      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
       ab = ab_next;
       aph = aph_next;
       if (++ab_next == acc_bufs) {
@@ -644,6 +653,20 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.NK = p.K / 128;
   p.RB = rows / 128;
   p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
+  // down GEMM: split the weight tiles into groups so that one group's slice of
+  // `out` (T rows x the group's 256-column blocks, fp32) stays within ~16 MB of
+  // L2 while every expert's atomic combine lands on it
+  p.MG = p.NM;
+  if (a.epi == 1) {
+    int groups = 1;
+    const double out_bytes = 4.0 * a.T * a.H;
+    while (out_bytes / groups > 16.0 * 1024 * 1024 && p.NM % (groups * 2) == 0) groups *= 2;
+    if (const char* env = std::getenv("MXMOE_MGROUPS")) {
+      const int v = std::atoi(env);
+      if (v >= 1 && p.NM % v == 0) groups = v;
+    }
+    p.MG = p.NM / groups;
+  }
   p.bn = a.bn;
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);

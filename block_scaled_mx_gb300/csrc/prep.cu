@@ -307,7 +307,16 @@ __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ 
   for (int e = tid; e <= E; e += blockDim.x) {
     int c = 0;
     if (e < E) {
-      for (int ch = 0; ch < nchunks; ++ch) c += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
+      // eight independent loads in flight at a time (the chunk counts sit in L2)
+      int ch = 0;
+      for (; ch + 8 <= nchunks; ch += 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch + u) * E + e]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) c += v[u];
+      }
+      for (; ch < nchunks; ++ch) c += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
     } else {
       c = T;
     }
@@ -345,7 +354,18 @@ __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ 
   if (nchunks > 1) {
     for (int e = tid; e < E; e += blockDim.x) {
       int base = scan[e];
-      for (int ch = 0; ch < nchunks; ++ch) {
+      int ch = 0;
+      for (; ch + 8 <= nchunks; ch += 8) {
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch + u) * E + e]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          sc.chunk_base[static_cast<int64_t>(ch + u) * E + e] = base;
+          base += v[u];
+        }
+      }
+      for (; ch < nchunks; ++ch) {
         sc.chunk_base[static_cast<int64_t>(ch) * E + e] = base;
         base += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
       }
@@ -410,7 +430,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
 // computes the whole permutation, which needs T <= kPermuteChunk.  It lets the
 // next grid (the gate/up GEMM, launched programmatically dependent) start its
 // set-up at once.
-template <int PER>
+template <int PER, bool PERMUTE>
 __global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
   extern __shared__ uint32_t bits[];
   __shared__ int s_last;
@@ -422,7 +442,7 @@ __global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
   const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
   for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
   for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (!a.permute) return;
+  if (!PERMUTE) return;
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(a.sc.done, 1u) == gridDim.x - 1;
@@ -438,21 +458,30 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
   int64_t blocks = (work + kPermuteChunk - 1) / kPermuteChunk;
   const int64_t route_blocks = (a.T + kPermuteChunk / 32 - 1) / (kPermuteChunk / 32);
   if (blocks < route_blocks) blocks = route_blocks;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * 4;
+  // eight 256-thread blocks per SM keep enough 16-byte loads in flight for
+  // the quantisation stream of a large batch
+  const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = a.permute ? static_cast<size_t>(kPermuteChunk / 32) * a.E * 4 + static_cast<size_t>(a.E + 2) * 4 : 0;
   const unsigned g = static_cast<unsigned>(blocks);
-  if (a.E <= 32) k_prologue<1><<<g, kPermuteChunk, smem, s>>>(a);
-  else if (a.E <= 128) k_prologue<4><<<g, kPermuteChunk, smem, s>>>(a);
-  else if (a.E <= 512) k_prologue<16><<<g, kPermuteChunk, smem, s>>>(a);
-  else {
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k_prologue<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-      if (e != cudaSuccess) return e;
+  if (a.permute) {
+    if (a.E <= 32) k_prologue<1, true><<<g, kPermuteChunk, smem, s>>>(a);
+    else if (a.E <= 128) k_prologue<4, true><<<g, kPermuteChunk, smem, s>>>(a);
+    else if (a.E <= 512) k_prologue<16, true><<<g, kPermuteChunk, smem, s>>>(a);
+    else {
+      if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k_prologue<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+      }
+      k_prologue<32, true><<<g, kPermuteChunk, smem, s>>>(a);
     }
-    k_prologue<32><<<g, kPermuteChunk, smem, s>>>(a);
+  } else {
+    if (a.E <= 32) k_prologue<1, false><<<g, kPermuteChunk, 0, s>>>(a);
+    else if (a.E <= 128) k_prologue<4, false><<<g, kPermuteChunk, 0, s>>>(a);
+    else if (a.E <= 512) k_prologue<16, false><<<g, kPermuteChunk, 0, s>>>(a);
+    else k_prologue<32, false><<<g, kPermuteChunk, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -313,3 +313,18 @@ def test_layer_parity_other_tile_width(name, bn, monkeypatch):
     assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
     rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
     assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+
+
+@pytest.mark.parametrize("name,groups", [("wide_e4m3", "2"), ("ragged_e4m3", "1"), ("decode_mxfp8", "4")])
+def test_layer_parity_down_tile_groups(name, groups, monkeypatch):
+    """The down GEMM with its weight tiles split into groups run one after the
+    other (the order the wide schedule uses so that the combine's atomics land on
+    an L2-sized slice of `out`)."""
+    monkeypatch.setenv("MXMOE_MGROUPS", groups)
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle_forward(L)
+    out = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
