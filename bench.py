@@ -177,7 +177,7 @@ def weight_bytes_per_expert(wl: W.Workload):
 
 def source_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "common.cuh"):
+    for f in ("gemm.cu", "ptx.cuh", "common.cuh", "api.cu"):
         h.update(open(os.path.join(ROOT, "block_scaled_mx_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 

@@ -21,7 +21,9 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 
 // Token-row tile width of the grouped GEMMs, chosen from the mean rows per
 // expert (known on the host, no device read).  The narrow decode schedule
-// (32 rows) streams weights with two accumulator buffers.  The wide prefill
+// (16 or 32 rows) streams weights with two accumulator buffers; 16-row tiles
+// (a few rows per expert) free shared memory for a third pipeline stage at the
+// price of a second tile for experts with more rows (the shared expert).  The wide prefill
 // schedule reuses each weight tile over 192 token rows with one accumulator
 // buffer: a block-scaled MMA costs about the same issue time for any N up to
 // 192, so doubling N over 96 (the widest tile with two buffers) outweighs the
@@ -30,9 +32,10 @@ int choose_bn(int T, int E, int k, int which) {
   const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
   if (env) {
     const int v = std::atoi(env);
-    if (v >= 32 && v <= 224 && v % 16 == 0) return v;
+    if (v >= 16 && v <= 224 && v % 16 == 0) return v;
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
+  if (mean_rows < 12.0) return 16;  // smaller B tiles leave room for a third stage
   if (mean_rows < 48.0) return 32;
   return 192;
 }

@@ -300,11 +300,13 @@ def test_layer_parity_other_stage_shape(name, kps, monkeypatch):
 
 
 @pytest.mark.parametrize("name,bn", [("wide_e4m3", "96"), ("wide_e4m3", "224"), ("wide_e2m1", "128"),
-                                     ("wide_e2m1", "160"), ("decode_mxfp8", "64"), ("ragged_e4m3", "192")])
+                                     ("wide_e2m1", "160"), ("decode_mxfp8", "64"), ("ragged_e4m3", "192"),
+                                     ("decode_mxfp4", "32"), ("ragged_e2m1", "16")])
 def test_layer_parity_other_tile_width(name, bn, monkeypatch):
     """Other token-tile widths than the shape's default: two accumulator buffers
     (96), one buffer with one or two K chunks per stage (128 .. 224), the gather4
-    schedule at 64 rows, and a wide tile on a shape whose experts hold few rows."""
+    schedule at 16, 32 and 64 rows, and a wide tile on a shape whose experts hold
+    few rows."""
     monkeypatch.setenv("MXMOE_BN", bn)
     wl = LAYER_CASES[name]
     L = build_layer(wl)
