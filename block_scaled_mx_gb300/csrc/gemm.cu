@@ -146,6 +146,22 @@ __device__ __forceinline__ bool warp_wait_bar(const Shared& sh, uint64_t* bar, u
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
+// One 128-wide K chunk of a tile: four K = 32 steps, each an MMA per row
+// block (gate and up, or two row blocks of W2) into its own accumulator;
+// `accum` turns on after the tile's first step.
+template <bool TWO>
+__device__ __forceinline__ void issue_chunk(uint32_t d0, uint32_t d1, uint32_t a_lo, uint32_t b_lo, uint32_t sf,
+                                            const uint32_t (&idesc)[4], uint32_t& accum) {
+#pragma unroll
+  for (int kb = 0; kb < 4; ++kb) {
+    mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
+    if (TWO)
+      mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
+                      sf + 16u, accum);
+    accum = 1u;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
@@ -365,31 +381,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t slot = s * kps;
-          for (uint32_t u = 0; u < kps; ++u, ++slot) {
-            const uint32_t sf = sf_base + slot * kSfColsPerChunk;
-            const uint64_t sfa_d = sfa_desc0 + (static_cast<uint64_t>(slot * (1024u >> 4)));
-            const uint32_t a_lo = a_lo0 + slot * (32768u >> 4);
-            const uint32_t b_lo = b_lo0 + slot * b_stride16;
+          // the stage's scale copies first, then all its MMAs back to back:
+          // the single issuing thread's work between two MMAs is tensor time
+          const uint32_t slot0 = s * kps;
+          for (uint32_t u = 0; u < kps; ++u) {
+            const uint32_t sf = sf_base + (slot0 + u) * kSfColsPerChunk;
+            const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((slot0 + u) * (1024u >> 4));
             tmem_cp_32x128b_warpx4(sf + 0u, sfa_d);
-            if (two) {
-              tmem_cp_32x128b_warpx4(sf + 8u, sfa_d + (512u >> 4));
-#pragma unroll
-              for (int kb = 0; kb < 4; ++kb) {
-                mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
-                                accum);
-                mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb],
-                                sf + 8u, sf + 16u, accum);
-                accum = 1u;
-              }
-            } else {
-#pragma unroll
-              for (int kb = 0; kb < 4; ++kb) {
-                mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u,
-                                accum);
-                accum = 1u;
-              }
-            }
+            if (two) tmem_cp_32x128b_warpx4(sf + 8u, sfa_d + (512u >> 4));
+          }
+          if (two) {
+            issue_chunk<true>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
+                              sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            if (kps == 2)
+              issue_chunk<true>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
+                                sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
+          } else {
+            issue_chunk<false>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
+                               sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            if (kps == 2)
+              issue_chunk<false>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
+                                 sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
           }
           mma_commit(smem_u32(&sh.empty[s]));
         }
