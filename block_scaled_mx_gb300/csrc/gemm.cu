@@ -122,13 +122,17 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int 
 }
 
 // Wait that also gives up when another role has aborted.
+// SLEEP: poll with a suspend-time hint (whole warps that wait long); the
+// single MMA-issuing thread polls without one, to resume the moment a stage
+// lands.
+template <bool SLEEP = true>
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
                                          unsigned long long limit_ns, int* status) {
   const uint32_t b = smem_u32(bar);
   if (mbar_try_wait(b, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait_sleep(b, parity, 20000u)) return true;
+    if (SLEEP ? mbar_try_wait_sleep(b, parity, 20000u) : mbar_try_wait(b, parity)) return true;
     if (*sh.abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       set_status(status, MX_ERR_TIMEOUT);
@@ -376,7 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs = 0;
             rph ^= 1u;
           }
-          if (!wait_bar(sh, &sh.full[s], ph, lim, status) || !wait_bar(sh, &sh.sfb_ready[s], ph, lim, status)) {
+          if (!wait_bar<false>(sh, &sh.full[s], ph, lim, status) ||
+              !wait_bar<false>(sh, &sh.sfb_ready[s], ph, lim, status)) {
             ok = false;
             break;
           }

@@ -179,6 +179,8 @@ LAYER_CASES = {
     "one_token": W.custom("one_token", T=1, H=256, I=128, E=4, k=2, fmt="e4m3"),
     "one_expert": W.custom("one_expert", T=5, H=128, I=128, E=1, k=1, fmt="e2m1"),
     "k_equals_e": W.custom("k_equals_e", T=9, H=256, I=256, E=4, k=4, fmt="e4m3"),
+    # the routing limits: 1024 routed experts (+1 shared), top-32
+    "max_routing": W.custom("max_routing", T=40, H=128, I=128, E=1024, k=32, fmt="e2m1"),
 }
 
 
