@@ -17,12 +17,13 @@
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
-//               unpacked to the 16-byte-aligned form by the TMA), their
-//               512-byte scale blocks (bulk copy), token rows (tensor map)
-//   warp 1      TMEM allocation; one thread issues tcgen05.cp for the weight
-//               scales and tcgen05.mma.kind::mxf8f6f4.block_scale
-//   warps 4-7   token-row scale staging: tcgen05.st of the B scale factors
-//               into every TMEM lane quarter
+//               unpacked to the 16-byte-aligned form by the TMA) and token
+//               rows (tensor map)
+//   warp 1      TMEM allocation; one thread issues
+//               tcgen05.mma.kind::mxf8f6f4.block_scale
+//   warps 4-7   scale staging: the weight and token-row scale factors of
+//               every stage, from global memory into every TMEM lane quarter
+//               with tcgen05.st
 //   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
 //               MXFP8 re-quantisation or weighted combine; warps w and w + 4
 //               share a TMEM lane quarter and take alternate column chunks
@@ -72,7 +73,7 @@ struct GemmParams {
   float* out;
   int* status;
   unsigned long long wait_limit_ns;
-  uint32_t off_a, off_b, off_sfa, off_meta, off_bar, off_epi;
+  uint32_t off_a, off_b, off_meta, off_bar, off_epi;
   uint32_t sf_col0;
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
   int pdl;          // see GemmArgs::pdl
@@ -90,7 +91,6 @@ struct Shared {
   volatile int* abort_flag;
   uint64_t* full;
   uint64_t* empty;
-  uint64_t* sfb_ready;
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
@@ -182,12 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + p.off_bar);
   sh.full = bars;
   sh.empty = bars + S;
-  sh.sfb_ready = bars + 2 * S;
-  sh.acc_full = bars + 3 * S;
-  sh.acc_empty = bars + 3 * S + 2;
-  sh.drain = bars + 3 * S + 4;
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
-  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 3 * S + 6);
+  sh.acc_full = bars + 2 * S;
+  sh.acc_empty = bars + 2 * S + 2;
+  sh.drain = bars + 2 * S + 4;
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 6);
 
   // ---- prologue: expert offsets, per-expert tile counts and their prefix
   const int E1 = p.E + 1;
@@ -196,9 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = p.offsets[i];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&sh.full[s]), 1);
+      // a stage is full when its TMA bytes have landed (producer: 1 arrival
+      // with the byte count) and the four scale-staging warps have put its
+      // scale factors into tensor memory (4 arrivals)
+      mbar_init(smem_u32(&sh.full[s]), 5);
       mbar_init(smem_u32(&sh.empty[s]), 1);
-      mbar_init(smem_u32(&sh.sfb_ready[s]), 4);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.acc_full[a]), 1);
@@ -271,8 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
       // the tile's two row blocks are prepared blocks 2m and 2m + 1 of each K
-      // chunk (gate and up block m in W1): one TMA box and one scale bulk copy
-      const bool two = 2 * tl.m + 1 < p.RB;
+      // chunk (gate and up block m in W1): one TMA box
       // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token)
       const int n4 = gather ? (tl.rows + 3) / 4 : 0;
       int tok[4] = {0, 0, 0, 0};
@@ -286,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
-      const uint32_t sfa_bytes = two ? 1024u : 512u;
-      const uint32_t bytes = (2u * p.a_tx + sfa_bytes + b_bytes) * static_cast<uint32_t>(kps);
+      const uint32_t bytes = (2u * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
@@ -301,12 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < kps; ++u) {
             const int kc = ks + u;
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
-            uint8_t* sfa_s = base + p.off_sfa + (su + u) * 1024u;
             // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
             // the TMA fills zeros and still counts the whole box)
             const int blk0 = (tl.e * NK + kc) * p.RB + 2 * tl.m;
             tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
-            bulk_load(smem_u32(sfa_s), p.w_scales + static_cast<size_t>(blk0) * 512u, sfa_bytes, full);
           }
         }
         if (!b_ready) {
@@ -351,13 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t rs = 0, rph = 0, ab = 0, aph = 0;
       const uint32_t afmt = p.afmt == MX_E4M3 ? kFmtE4M3 : kFmtE2M1;
       const uint32_t sf_base = tbase + p.sf_col0;
-      const uint32_t sfa_base = smem_u32(base + p.off_sfa);
       const uint32_t a_base = smem_u32(base + p.off_a);
       const uint32_t b_base = smem_u32(base + p.off_b);
       const uint32_t b_stride16 = static_cast<uint32_t>(p.bn) * (128u >> 4);
       const uint32_t kps = static_cast<uint32_t>(p.kps);
       // descriptors of slot 0 (start address field is addr >> 4; slots add to it)
-      const uint64_t sfa_desc0 = smem_desc(sfa_base, 0, 128, kSwizzleNone);
       const uint32_t a_lo0 = desc_lo_sw128(a_base);
       const uint32_t b_lo0 = desc_lo_sw128(b_base);
       bool ok = true;
@@ -380,21 +375,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs = 0;
             rph ^= 1u;
           }
-          if (!wait_bar<false>(sh, &sh.full[s], ph, lim, status) ||
-              !wait_bar<false>(sh, &sh.sfb_ready[s], ph, lim, status)) {
+          if (!wait_bar<false>(sh, &sh.full[s], ph, lim, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // the stage's scale copies first, then all its MMAs back to back:
-          // the single issuing thread's work between two MMAs is tensor time
+          // all the stage's MMAs back to back (its scale factors are already in
+          // tensor memory): the single issuing thread's work between two MMAs
+          // is tensor time
           const uint32_t slot0 = s * kps;
-          for (uint32_t u = 0; u < kps; ++u) {
-            const uint32_t sf = sf_base + (slot0 + u) * kSfColsPerChunk;
-            const uint64_t sfa_d = sfa_desc0 + static_cast<uint64_t>((slot0 + u) * (1024u >> 4));
-            tmem_cp_32x128b_warpx4(sf + 0u, sfa_d);
-            if (two) tmem_cp_32x128b_warpx4(sf + 8u, sfa_d + (512u >> 4));
-          }
           if (two) {
             issue_chunk<true>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
                               sf_base + slot0 * kSfColsPerChunk, idesc, accum);
@@ -422,24 +411,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(sh.drain), 0, 100000000ull);
     }
   } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
-    // ================================================================ B scale staging
-    // Per stage, the token-row scales of its K chunks are read from global
-    // memory (one 32-bit word per row and chunk; L2-resident, and issued before
-    // the slot is free so their latency overlaps the wait) and stored with
-    // tcgen05.st into this warp's TMEM lane quarter (all four quarters hold the
-    // same words).
+    // ================================================================ scale staging
+    // Per stage: the weight (A) scale blocks of the tile's two row blocks (one
+    // 16-byte word per lane and block, already in the tensor-memory order) and
+    // the token-row (B) scales (one 32-bit word per row and chunk) are read from
+    // global memory -- issued before the slot is free: the ring gives them S
+    // stages of lead -- and stored with tcgen05.st into this warp's TMEM lane
+    // quarter (all four quarters hold the same words, the layout the block-
+    // scaled MMA reads).  The warp then arrives on the stage's full barrier.
     const int q = warp & 3;
     const int K32 = p.K / 32;
     const uint32_t S_ = static_cast<uint32_t>(S);
     const int kps = p.kps, bn = p.bn;
     const unsigned long long lim = p.wait_limit_ns;
     int* const status = p.status;
-    const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0 + 16u;
+    const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0;
+    const uint4* const wsc = reinterpret_cast<const uint4*>(p.w_scales);
     uint32_t rs = 0, rph = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const bool two = 2 * tl.m + 1 < p.RB;
       // rows 32j + lane of this tile: their scale rows (null: a padding row)
       const uint32_t* rowp[8];
 #pragma unroll
@@ -465,10 +458,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           rph ^= 1u;
         }
         uint32_t bw[2][8];
+        uint4 a0[2], a1[2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int u = 0; u < 2; ++u) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) bw[u][j] = (u < kps && rowp[j]) ? __ldg(rowp[j] + ks + u) : 0x7F7F7F7Fu;
+          a0[u] = a1[u] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+          if (u < kps) {
+            const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + ks + u) * p.RB + 2 * tl.m) * 32;
+            a0[u] = __ldg(blk + lane);
+            if (two) a1[u] = __ldg(blk + 32 + lane);
+          }
+        }
         if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
@@ -476,17 +477,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           if (u < kps) {
-            // column j of the B scale block holds rows 32j + lane (j < 8: N <= 256)
+            // chunk slot: A scales of row block 2m at +0, of 2m + 1 at +8, B at
+            // +16 (column j of a block holds rows 32j + lane; B: j < 8, N <= 256)
             const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + u) * kSfColsPerChunk;
             __syncwarp();
-            if (bn > 128) tmem_st_32x32b_x8(col, bw[u]);
-            else tmem_st_32x32b_x4(col, bw[u][0], bw[u][1], bw[u][2], bw[u][3]);
+            tmem_st_32x32b_x4(col + 0u, a0[u].x, a0[u].y, a0[u].z, a0[u].w);
+            tmem_st_32x32b_x4(col + 8u, a1[u].x, a1[u].y, a1[u].z, a1[u].w);
+            if (bn > 128) tmem_st_32x32b_x8(col + 16u, bw[u]);
+            else tmem_st_32x32b_x4(col + 16u, bw[u][0], bw[u][1], bw[u][2], bw[u][3]);
           }
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.sfb_ready[s]));
+        if (lane == 0) mbar_arrive(smem_u32(&sh.full[s]));
       }
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
@@ -717,7 +721,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     *acc_bufs = (4u * static_cast<uint32_t>(p.bn) + 2u * kSfColsPerChunk * kps <= kTmemCols) ? 2 : 1;
     *sf_col0 = 2u * static_cast<uint32_t>(*acc_bufs) * static_cast<uint32_t>(p.bn);
     if (*sf_col0 + 2u * kSfColsPerChunk * kps > kTmemCols) return 0;
-    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u + 1024u) * static_cast<uint32_t>(kps);
+    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u) * static_cast<uint32_t>(kps);
     if (static_cast<uint32_t>(max_smem) <= fixed) return 0;
     int st = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
     if (st > kMaxStages) st = kMaxStages;
@@ -750,8 +754,6 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   off += static_cast<uint32_t>(stages * p.kps) * 32768u;
   p.off_b = off;
   off += static_cast<uint32_t>(stages * p.kps) * p.bn * 128u;
-  p.off_sfa = off;
-  off += static_cast<uint32_t>(stages * p.kps) * 1024u;
   p.off_meta = off;
   off += meta_bytes;
   p.off_bar = off;
