@@ -522,7 +522,7 @@ cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
 // (e * NK + kc) * RB + rb': for one K chunk, all row blocks of an expert are
 // adjacent, so the two row blocks a GEMM tile multiplies (gate block m and up
 // block m, interleaved as rb' = 2m and 2m + 1 in W1; row blocks 2m and 2m + 1 in
-// W2) arrive with one TMA box and their scale blocks with one bulk copy.
+// W2) arrive with one TMA box.
 PreparedLayout prepared_layout(int E1, int rows, int K, int fmt, int interleave) {
   PreparedLayout L;
   L.E1 = E1;
