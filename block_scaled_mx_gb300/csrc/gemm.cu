@@ -451,6 +451,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           rowp[j] = reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32);
         }
       }
+      // warm L2 with the tile's weight-scale blocks (128-byte lines, 4 per
+      // block, one or two blocks per chunk): the per-stage loads below then hit
+      // L2 instead of waiting on DRAM
+      {
+        const int lines = two ? 8 : 4;
+        const int sft = tid - kWarpSf0 * 32;
+        for (int i = sft; i < NK * lines; i += 128) {
+          const int kc = i / lines, line = i - kc * lines;
+          const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * tl.m) * 32;
+          prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
+        }
+      }
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (++rs == S_) {
