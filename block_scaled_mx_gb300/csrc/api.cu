@@ -24,10 +24,11 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 // (16 or 32 rows) streams weights with two accumulator buffers; 16-row tiles
 // (a few rows per expert) free shared memory for a third pipeline stage at the
 // price of a second tile for experts with more rows (the shared expert).  The wide prefill
-// schedule reuses each weight tile over 192 token rows with one accumulator
-// buffer: a block-scaled MMA costs about the same issue time for any N up to
-// 192, so doubling N over 96 (the widest tile with two buffers) outweighs the
-// epilogue no longer overlapping the MMAs.  `which`: 0 gate/up, 1 down.
+// schedule reuses each weight tile over many token rows; for the gate/up GEMM
+// 192 with one accumulator buffer: a block-scaled MMA costs about the same issue
+// time for any N up to 192, so doubling N over 96 (the widest tile with two
+// buffers) outweighs the epilogue no longer overlapping the MMAs.
+// `which`: 0 gate/up, 1 down.
 int choose_bn(int T, int E, int k, int which) {
   const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
   if (env) {
@@ -37,7 +38,9 @@ int choose_bn(int T, int E, int k, int which) {
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
   if (mean_rows < 12.0) return 16;  // smaller B tiles leave room for a third stage
   if (mean_rows < 48.0) return 32;
-  return 192;
+  // down GEMM: two accumulator buffers at 96 rows hide its atomic-combine
+  // epilogue behind the next tile's MMAs, which beats the fewer MMAs of 192
+  return which == 0 ? 192 : 96;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
