@@ -188,11 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 6);
 
-  // ---- prologue: expert offsets, per-expert tile counts and their prefix
+  // ---- set-up that needs nothing from the previous grid (barriers, tensor
+  // memory) runs before waiting on it; then the expert offsets, per-expert
+  // tile counts and their prefix
   const int E1 = p.E + 1;
-  if (p.pdl == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.pdl != 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = p.offsets[i];
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // a stage is full when its TMA bytes have landed (producer: 1 arrival
@@ -213,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(sh.tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  if (p.pdl == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.pdl != 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (int i = tid; i < E1 + 1; i += blockDim.x) sh.offs[i] = p.offsets[i];
   __syncthreads();
   // tile prefix: each thread owns a run of experts, warp 0..11 shuffle-scan
   {
