@@ -570,7 +570,8 @@ __global__ void __launch_bounds__(256) k_prepare_codes(const uint4* __restrict__
 
 // scales: one thread per 32-bit word of a 512-byte block: lane l, word j holds
 // the four k-blocks of row 32*j + l (the tensor-memory scale-factor layout of
-// the block-scaled MMA, copied in by tcgen05.cp 32x128b.warpx4).
+// the block-scaled MMA: a lane's 16-byte word is what it stores into its
+// tensor-memory lane with tcgen05.st 32x32b.x4).
 __global__ void __launch_bounds__(256) k_prepare_scales(const uint8_t* __restrict__ src, int rows,
                                                         int K32, int RB, int NK, int interleave,
                                                         int64_t total_words, uint32_t* __restrict__ dst) {

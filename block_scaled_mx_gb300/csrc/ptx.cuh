@@ -71,11 +71,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-// ---------------------------------------------------------------- proxies
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- TMA / bulk
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
@@ -98,28 +93,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-      : "memory");
-}
-// L2 prefetch of one tensor-map box / of a contiguous range (no shared memory
-// written, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(z)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
-               "r"(bytes)
-               : "memory");
-}
-// Untiled bulk copy global -> shared; both addresses 16-byte aligned, size a
-// multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 // One 128-byte line of global memory into L2 (no data returned).
@@ -153,20 +126,10 @@ __device__ __forceinline__ void tc_fence_after() {
 // D[tmem] (+)= (A * 2^sfa) x (B * 2^sfb), one MX block of K = 32 per call.
 // A and B come from shared memory through matrix descriptors; the E8M0 scale
 // factors come from tensor memory.  `accumulate` = 0 overwrites D.
-__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                             uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
-      : "memory");
-}
-// Same MMA with the two shared-memory descriptors given as their low 32-bit
-// halves and one shared high half (stride, version, swizzle): the issuing
-// thread then spends one add per operand per K step instead of rebuilding
-// 64-bit descriptors.  No memory clobber: the MMA reads shared memory
+// The two shared-memory descriptors are given as their low 32-bit halves and
+// one shared high half (stride, version, swizzle): the issuing thread then
+// spends one add per operand per K step instead of rebuilding 64-bit
+// descriptors.  No memory clobber: the MMA reads shared memory
 // asynchronously, ordered by mbarriers and tcgen05 fences, not by the
 // compiler, and a clobber would make the issuing thread reload values between
 // MMAs (the thread's instruction count per MMA sets the issue rate).
@@ -181,8 +144,11 @@ __device__ __forceinline__ void mma_mxf8f6f4_lo(uint32_t d_tmem, uint32_t a_lo, 
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], ad, bd, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
       "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem), "r"(desc_hi));
 }
-// Low / high halves of the K-major, 128-byte-swizzled operand descriptor with
-// 8-row groups 1024 bytes apart (see smem_desc).
+// Low / high halves of the tcgen05 shared-memory matrix descriptor of a
+// K-major, 128-byte-swizzled operand with 8-row groups 1024 bytes apart: start
+// address >> 4 in bits 0-13, leading byte offset >> 4 (16 B) in 16-29, stride
+// byte offset >> 4 (1024 B) in 32-45, the fixed version bit 46, swizzle mode 2
+// (128 B) in 61-63.
 __device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t addr) {
   return ((addr >> 4) & 0x3FFFu) | (1u << 16);
 }
@@ -193,11 +159,6 @@ constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // 12
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-// Shared -> tensor memory: 32 rows x 128 bit, replicated into all four lane
-// quarters (lane l of every quarter receives row l).
-__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc));
 }
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t r0, uint32_t r1,
                                                   uint32_t r2, uint32_t r3) {
@@ -236,22 +197,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float4 v) {
 }
 
 // ---------------------------------------------------------------- descriptors
-// Shared-memory matrix descriptor (tcgen05 form): start address, leading and
-// stride byte offsets (all >> 4), the fixed version field 0b001 at bit 46 and
-// the swizzle mode in bits 61..63 (2 = 128-byte swizzle, 0 = none).
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
-                                              uint32_t swizzle) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-  d |= 1ull << 46;
-  d |= static_cast<uint64_t>(swizzle & 7u) << 61;
-  return d;
-}
-constexpr uint32_t kSwizzle128B = 2;
-constexpr uint32_t kSwizzleNone = 0;
-
 // Element-type codes of the mxf8f6f4 instruction descriptor.
 constexpr uint32_t kFmtE4M3 = 0;
 constexpr uint32_t kFmtE2M1 = 5;
@@ -265,14 +210,6 @@ __host__ __device__ __forceinline__ uint32_t idesc_mx(uint32_t a_fmt, uint32_t b
   return ((sfb_id & 3u) << 4) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10) |
          (((N >> 3) & 0x3Fu) << 17) | (1u << 23) | (((M >> 4) & 0x1Fu) << 24) |
          ((sfa_id & 3u) << 29);
-}
-
-// Byte offset of byte `b` (0..127) of row `r` inside a K-major tile whose rows
-// are 128 bytes and which uses the 128-byte swizzle (16-byte chunks XOR-ed with
-// the row index inside each 8-row, 1024-byte atom).  The tile base must be
-// 1024-byte aligned.
-__host__ __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t b) {
-  return r * 128u + ((((b >> 4) ^ (r & 7u)) & 7u) << 4) + (b & 15u);
 }
 
 }  // namespace mxk
