@@ -32,6 +32,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 
@@ -53,6 +54,7 @@ __host__ __device__ constexpr uint32_t epi_buf_bytes(int epi) { return epi == 0 
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
 constexpr int kMaxStages = 8;
+constexpr int kMaxDevices = 64;
 
 struct GemmParams {
   int epi, afmt, T, H, I, E, k;
@@ -813,9 +815,17 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
 
-  cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is per device and only ever raised: skip the
+  // driver call when a launch on this device already allowed this much
+  {
+    static std::atomic<int> smem_allowed[kMaxDevices];
+    if (dev < 0 || dev >= kMaxDevices || smem_allowed[dev].load(std::memory_order_relaxed) < static_cast<int>(smem)) {
+      cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < kMaxDevices) smem_allowed[dev].store(static_cast<int>(smem), std::memory_order_relaxed);
+    }
+  }
   // upper bound on tiles: NM * sum_e ceil(count_e / bn) <= NM * (E + 1 + rows / bn)
   const long long bound =
       static_cast<long long>(p.NM) * (a.E + 1 + (a.n_rows + p.bn - 1) / p.bn);
