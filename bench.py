@@ -454,8 +454,16 @@ def run_gpu(args, wl, rank, world, local):
     if world == 1 and not args.no_cpu_baseline:
         try:
             runner = OracleRunner(wl)
-            rate, sample = runner.rate(args.cpu_budget_s)
+            rate, sample = runner.rate(args.cpu_budget_s * 2 / 3)
             cpu = {"value": rate, "unit": "tokens/s", "cores": runner.threads, "kind": "oracle", "sample": sample}
+            if wl.T <= 64:  # small configurations: also one core, the oracle's per-core speed
+                try:
+                    runner.oracle.set_threads(1)
+                    rate1, sample1 = runner.rate(args.cpu_budget_s / 3, n_tokens=1)
+                finally:
+                    runner.oracle.set_threads(0)
+                cpu["value_1core"] = rate1
+                cpu["sample_1core"] = sample1
         except Exception as exc:  # the GPU number stands without it
             cpu = {"value": None, "unit": "tokens/s", "cores": None, "kind": "oracle", "sample": f"failed: {exc}"}
     fused = T <= 256 and (T * (k + 1)) / (E + 1) < 48

@@ -55,6 +55,8 @@ def lib():
         L.orc_permute.argtypes = [P, i32, i32, i32, P, P, P]
         L.orc_expert_layer.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
                                        P, P, P, P]
+        L.orc_set_threads.argtypes = [i32]
+        L.orc_set_threads.restype = None
         _lib = L
     return _lib
 
@@ -252,3 +254,9 @@ def moe_forward(x_bits, logits, k: int, w1c, w1s, w2c, w2s, fmt: int, I: int, to
                        want_noq=want_noq)
     res.update(act_codes=act_codes, act_scales=act_scales, ids=ids, topk_w=w)
     return res
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads for the oracle's parallel loops (n <= 0: all cores).
+    Results are identical for any thread count."""
+    lib().orc_set_threads(int(n))

@@ -28,6 +28,7 @@
  * Non-finite inputs are a precondition violation and return ORC_ERR_NONFINITE.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -435,4 +436,12 @@ int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T,
 done:
   free(row_of); free(xd); free(w1d); free(w2d); free(slot_tok); free(slot_j); free(ybuf); free(ybuf_noq);
   return st;
+}
+
+/* Number of OpenMP threads the oracle's parallel loops use from now on (the
+   results do not depend on it: every output is computed by one thread in index
+   order).  n <= 0 restores the runtime default. */
+void orc_set_threads(int n) {
+  if (n > 0) omp_set_num_threads(n);
+  else omp_set_num_threads(omp_get_num_procs());
 }

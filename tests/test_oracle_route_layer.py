@@ -205,3 +205,20 @@ def test_layer_rejects_missing_expert(orc):
     w1c[int(ids[0, 0])] = None
     with pytest.raises(ValueError):
         orc.expert_layer(act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I)
+
+
+def test_layer_result_does_not_depend_on_thread_count(orc):
+    """Every output of the oracle is computed by one thread in index order, so
+    one thread and all cores give bit-identical layers (the benchmark times both)."""
+    rng = np.random.default_rng(5)
+    fmt = orc.E4M3
+    act_c, act_s, ids, w, w1c, w1s, w2c, w2s = _random_layer(orc, rng, 9, 64, 64, 6, 3, fmt)
+    try:
+        orc.set_threads(1)
+        one = orc.expert_layer(act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, 64, want_h=True)
+        orc.set_threads(0)
+        many = orc.expert_layer(act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, 64, want_h=True)
+    finally:
+        orc.set_threads(0)
+    assert np.array_equal(one["out"], many["out"])
+    assert np.array_equal(one["h_codes"], many["h_codes"])
