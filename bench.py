@@ -176,9 +176,16 @@ def weight_bytes_per_expert(wl: W.Workload):
 
 
 def source_hash():
+    """Hash of the code (comments and blank lines dropped) of the sources the
+    dominant kernel and its launch schedule are built from."""
+    import re
+
     h = hashlib.sha256()
     for f in ("gemm.cu", "ptx.cuh", "common.cuh", "api.cu"):
-        h.update(open(os.path.join(ROOT, "block_scaled_mx_gb300", "csrc", f), "rb").read())
+        text = open(os.path.join(ROOT, "block_scaled_mx_gb300", "csrc", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        h.update("\n".join(ln for ln in lines if ln.strip()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,9 +11,12 @@
 // tile), the expert's token rows are the B operand (N = the tile's token count
 // rounded up to 16, at most `bn`), so a decode tile with two tokens still runs
 // full-width M = 128 MMAs while streaming weights ("swap-AB").  Tiles are
-// (expert, weight rows, token rows), expert-major, handed out round-robin to
-// one CTA per SM; per-expert token counts are read from the device-side
-// permutation offsets, so nothing waits on the host.
+// (expert, token rows, weight rows), expert-major (the down GEMM of a large
+// batch runs its weight tiles in groups, one after the other), handed out
+// round-robin to one CTA per SM; per-expert token counts are read from the
+// device-side permutation offsets, so nothing waits on the host.  A pipeline
+// stage is full once its TMA bytes have landed and the scale-staging warps
+// have put its scale factors into tensor memory.
 //
 // Warp roles (512 threads):
 //   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
