@@ -26,38 +26,48 @@ E4M3 = 0
 E2M1 = 1
 
 
+def compile_library(src: str, out: str) -> str:
+    """gcc, -O2, OpenMP, no fast-math: ``src`` (C11) -> shared library ``out``."""
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
-    """Compile ``mx_oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP, no fast-math)."""
+    """Compile ``mx_oracle.c`` into ``liboracle.so``."""
     if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
-        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", _LIB_PATH, _SRC, "-lm"]
-        subprocess.run(cmd, check=True)
+        compile_library(_SRC, _LIB_PATH)
     return _LIB_PATH
+
+
+def _bind(L):
+    """Declare the C signatures on a loaded oracle library and return it."""
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int, ctypes.c_int64
+    L.orc_decode_e4m3.restype = ctypes.c_double
+    L.orc_decode_e4m3.argtypes = [i32]
+    L.orc_decode_e2m1.restype = ctypes.c_double
+    L.orc_decode_e2m1.argtypes = [i32]
+    L.orc_decode_e8m0.restype = ctypes.c_double
+    L.orc_decode_e8m0.argtypes = [i32]
+    L.orc_quantize_block.argtypes = [P, i32, i32, P, P]
+    L.orc_quantize_rows.argtypes = [P, i64, i64, i32, P, P]
+    L.orc_quantize_bf16.argtypes = [P, i64, i64, P, P]
+    L.orc_quantize_f32.argtypes = [P, i64, i64, i32, P, P]
+    L.orc_route_topk.argtypes = [P, i32, i32, i32, P, P]
+    L.orc_permute.argtypes = [P, i32, i32, i32, P, P, P]
+    L.orc_expert_layer.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
+                                   P, P, P, P]
+    L.orc_set_threads.argtypes = [i32]
+    L.orc_set_threads.restype = None
+    return L
 
 
 def lib():
     global _lib
     if _lib is None:
         build()
-        L = ctypes.CDLL(_LIB_PATH)
-        P = ctypes.c_void_p
-        i32, i64 = ctypes.c_int, ctypes.c_int64
-        L.orc_decode_e4m3.restype = ctypes.c_double
-        L.orc_decode_e4m3.argtypes = [i32]
-        L.orc_decode_e2m1.restype = ctypes.c_double
-        L.orc_decode_e2m1.argtypes = [i32]
-        L.orc_decode_e8m0.restype = ctypes.c_double
-        L.orc_decode_e8m0.argtypes = [i32]
-        L.orc_quantize_block.argtypes = [P, i32, i32, P, P]
-        L.orc_quantize_rows.argtypes = [P, i64, i64, i32, P, P]
-        L.orc_quantize_bf16.argtypes = [P, i64, i64, P, P]
-        L.orc_quantize_f32.argtypes = [P, i64, i64, i32, P, P]
-        L.orc_route_topk.argtypes = [P, i32, i32, i32, P, P]
-        L.orc_permute.argtypes = [P, i32, i32, i32, P, P, P]
-        L.orc_expert_layer.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
-                                       P, P, P, P]
-        L.orc_set_threads.argtypes = [i32]
-        L.orc_set_threads.restype = None
-        _lib = L
+        _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 
