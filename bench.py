@@ -247,6 +247,23 @@ class OracleRunner:
         return done / spent, sample
 
 
+# ------------------------------------------------------------------ replicas
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank gets the maximum of ``ms`` over the
+    process group (a tensor on ``device``: the GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, T: int, ms: float) -> float:
+    """Tokens/s of the whole job: each of ``world`` replicas runs the layer on
+    its own T tokens, and the job takes as long as the slowest one (``ms``)."""
+    return world * T / (ms * 1e-3)
+
+
 # ------------------------------------------------------------------ main arms
 def run_reference(args, wl, rank, world):
     if rank != 0:
@@ -389,11 +406,8 @@ def run_gpu(args, wl, rank, world, local):
     fused_ms = np.array([a.elapsed_time(b) for a, b in fev])
     ms = float(fused_ms.mean())
     steps_ms = float(per.sum(1).mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms * 1e-3)
+    ms = max_over_ranks(ms, world, dev)
+    value = replica_throughput(world, T, ms)
 
     # ---- e2e through the public single call with host buffers
     x_h = x.cpu().pin_memory()
@@ -420,11 +434,7 @@ def run_gpu(args, wl, rank, world, local):
         e1.record(stream)
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        t = torch.tensor([e2e], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
     if mx.moe_get_status(layer.workspace(T)):
         raise RuntimeError("device status error in moe_forward")
 
@@ -496,7 +506,7 @@ def run_gpu(args, wl, rank, world, local):
         "kernels_ms": {"quantize": float(per[:, 0].mean()), "topk": float(per[:, 1].mean()),
                        "permute+zero": float(per[:, 2].mean()), "gateup_call": gemm1_ms, "down_call": gemm2_ms,
                        "step_calls_total": steps_ms},
-        "e2e": {"value": world * T / (e2e * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
+        "e2e": {"value": replica_throughput(world, T, e2e), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 4, "ms_per_step": e2e},
         "cpu_baseline": cpu,
         "clocks": clk.summary(),
