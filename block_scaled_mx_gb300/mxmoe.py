@@ -85,10 +85,17 @@ def status_string(status: int) -> str:
 
 
 def _ptr(t) -> Optional[int]:
+    """A tensor's device address.  The library reads every buffer as dense
+    row-major device memory, so a strided view or a host tensor is refused
+    here rather than read wrongly.  An int is taken as a raw device pointer."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got shape {tuple(t.shape)} strides {t.stride()}")
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
     return t.data_ptr()
 
 

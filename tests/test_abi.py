@@ -89,3 +89,20 @@ def test_product_does_not_import_oracle():
                 txt = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, f
                 assert "mx_oracle" not in txt, f
+
+
+def test_binding_refuses_host_and_strided_tensors(L):
+    """The binding hands the library plain device addresses: a host tensor or a
+    strided view is refused before any call reaches the library."""
+    import torch
+
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    host = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        mx.mx_quantize_act(host, None, None)
+    meta = torch.empty(64, 4, dtype=torch.bfloat16, device="meta").t()
+    assert not meta.is_contiguous()
+    with pytest.raises(ValueError, match="contiguous"):
+        mx._ptr(meta)
+    assert mx._ptr(None) is None and mx._ptr(4096) == 4096
