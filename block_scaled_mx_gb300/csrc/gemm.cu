@@ -259,10 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTma) {
     // ================================================================ producer
-    // Lane 0 arms each stage and issues the weight-block TMA loads and their
-    // scale-block bulk copies; the token rows come either as one 2-D box (down GEMM: h rows are contiguous)
-    // or as TMA gather4 loads of four token rows each, one per lane (gate/up:
-    // the tokens of an expert are scattered over the activation matrix).
+    // Lane 0 arms each stage and issues the weight-block TMA loads; the token
+    // rows come either as one 2-D box of slot-ordered rows (the down GEMM's h,
+    // or activation rows the wide schedule gathered into slot order first) or
+    // as TMA gather4 loads of four token rows each, one per lane (the narrow
+    // gate/up schedule: an expert's tokens are scattered over the activation
+    // matrix).  The scale factors are staged by the scale warps.
     if (lane == 0) {
       prefetch_tensormap(&tm_a);
       prefetch_tensormap(&tm_b);
@@ -753,8 +755,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     return st >= 2 ? st : 0;
   };
   // Two 128-wide K chunks per pipeline stage when two such stages fit: the
-  // fixed per-stage costs of the single MMA-issuing thread (barrier waits,
-  // fences, scale copies, commit) are then paid once per 256 K.
+  // fixed per-stage costs of the single MMA-issuing thread (barrier wait,
+  // fence, commit) are then paid once per 256 K.
   p.kps = 1;
   if ((p.K / 128) % 2 == 0) {
     int ab;

@@ -1,7 +1,8 @@
 // Thin inline-PTX wrappers for the Blackwell (sm_103a) primitives the MX MoE
-// kernels use: mbarriers, TMA / bulk copies, tcgen05 (TMEM allocation, block-
-// scaled MMA, TMEM <-> register/shared copies) and the shared-memory matrix and
-// instruction descriptors.  Bit layouts follow the PTX ISA (tcgen05 "Matrix
+// kernels use: mbarriers, TMA tensor loads (tiled and gather4), tcgen05 (TMEM
+// allocation, block-scaled MMA, TMEM <-> register loads and stores), L2
+// prefetch, vector reductions, and the shared-memory matrix and instruction
+// descriptors.  Bit layouts follow the PTX ISA (tcgen05 "Matrix
 // Descriptors" and "Instruction descriptor" tables); nothing here is
 // shape-specific.
 #pragma once
@@ -71,7 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   }
 }
 
-// ---------------------------------------------------------------- TMA / bulk
+// ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             uint32_t bar) {
   asm volatile(
