@@ -16,8 +16,12 @@
 //     them) race on the shared array -- order them on one stream;
 //   * the first call on each device looks the array's device address up
 //     (cudaGetSymbolAddress with that device current) and caches it; make that
-//     first call before any stream capture begins.
+//     first call before any stream capture begins.  The cache is keyed on the
+//     device's current CUDA context, so after cudaDeviceReset (a new context,
+//     a new address) the next call looks the address up again.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <cstdint>
 #include <mutex>
 
@@ -33,22 +37,58 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_permute_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct CachedAddress {
+  unsigned long long ctx_id;  // context the address belongs to (0: none cached)
+  void* addr;
+};
+CachedAddress g_scratch_addr[kMaxDevices] = {};
+
+// Process-unique id of the calling thread's current CUDA context, or 0 when it
+// cannot be had (then nothing is cached).  The driver calls come through the
+// runtime's entry-point query, so the library needs no link against libcuda.
+unsigned long long current_context_id(int dev) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) {
+    // no context current on this thread yet: make the device's primary
+    // context current (what the runtime would do on its first call)
+    if (cudaSetDevice(dev) != cudaSuccess || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  }
+  unsigned long long id = 0;
+  return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 // Device address of g_permute_scratch on the current device.  In host code the
 // array's name is only a handle for the runtime: the address the kernels need
-// comes from cudaGetSymbolAddress, looked up once per device.
+// comes from cudaGetSymbolAddress, looked up once per device and context.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MX_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MX_ERR_UNSUPPORTED;
+  const unsigned long long ctx = current_context_id(dev);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  CachedAddress& c = g_scratch_addr[dev];
+  if (ctx == 0 || c.ctx_id != ctx || !c.addr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MX_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    c.addr = p;
+    c.ctx_id = ctx;
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return MX_OK;
 }
 

@@ -420,7 +420,12 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || nchunks == 1) return e;
   k_permute_scatter<<<nchunks, kPermuteChunk, 0, s>>>(ids, T, E, k, offsets, sorted_slot, sc);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  // the counting pass ran and left its last-block counter at nchunks; the
+  // scatter, which puts it back to zero, did not start: reset it here so the
+  // next call on this workspace still finds its last block
+  if (e != cudaSuccess) cudaMemsetAsync(sc.done, 0, sizeof(unsigned), s);
+  return e;
 }
 
 // ------------------------------------------------------------------ fused prologue

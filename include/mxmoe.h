@@ -132,7 +132,9 @@ MX_API int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* co
  *  - The array is shared by every call on a device and keeps the last call's
  *    contents; calls that overlap on the GPU race, so keep them on one stream.
  *  - The first call on a device looks up the array's device address; make it
- *    before any stream capture.  Device-side id errors are not reported.
+ *    before any stream capture.  The address is kept per device and CUDA
+ *    context: after cudaDeviceReset the next call looks it up again.
+ *    Device-side id errors are not reported.
  *  - Allocates nothing: no cudaMalloc/cudaFree or allocating library call. */
 MX_API int moe_permute_no_alloc(const int32_t* topk_ids, int T, int E, int k, int32_t* counts,
                                 int32_t* offsets, int32_t* sorted_slot, mx_stream_t stream);

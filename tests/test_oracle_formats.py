@@ -157,3 +157,74 @@ def test_nonfinite_is_rejected(orc):
     v[3] = np.inf
     with pytest.raises(ValueError):
         orc.quantize_block(v, orc.E2M1)
+
+
+def _brute_force_mx(w64, grid, emax, signbit):
+    """MX quantisation of fp64 rows written independently of the oracle: block
+    exponent from numpy's frexp, elements divided by 2^exponent, nearest value
+    of `grid` (the element format's non-negative magnitudes in code order) by
+    exhaustive search, ties to the even code, sign kept."""
+    rows, K = w64.shape
+    blocks = w64.reshape(rows, K // 32, 32)
+    amax = np.abs(blocks).max(-1)
+    _, ex = np.frexp(amax)
+    s = np.where(amax > 0, ex - 1 - emax, -127).clip(-127, 127)
+    q = blocks * np.exp2(-s.astype(np.float64))[..., None]
+    d = np.abs(np.abs(q)[..., None] - grid)            # [rows, K/32, 32, n_codes]
+    best = d.min(-1, keepdims=True)
+    cand = d == best
+    n = grid.size
+    # the lowest even code among the nearest, else the lowest code
+    even = cand & (np.arange(n) % 2 == 0)
+    code = np.where(even.any(-1), np.argmax(even, -1), np.argmax(cand, -1))
+    code = code | np.where(np.signbit(q), signbit, 0)
+    return code.reshape(rows, K).astype(np.uint8), (s + 127).astype(np.uint8)
+
+
+@pytest.mark.parametrize("fmt_name", ["e4m3", "e2m1"])
+def test_weight_quantiser_matches_brute_force(orc, fmt_name):
+    """fp32 weight rows -> MX codes and scales, against a brute-force
+    quantisation built from torch's E4M3 value table (or the OCP E2M1 table)
+    and numpy's frexp.  The row count is odd and exceeds the oracle's thread
+    count, and K = 96 is not a power of two, so a wrong row stride, a wrong row
+    copy or a lost row in the parallel split shows up."""
+    import os
+
+    rows, K = 2 * (os.cpu_count() or 1) + 5, 96
+    g = torch.Generator().manual_seed(11)
+    w = torch.randn(rows, K, generator=g) * torch.exp(torch.randn(rows, 1, generator=g) * 3) * 0.02
+    w[0, :32] = 0.0
+    w[1, 4] = -1e-30            # negative that rounds to -0 in its block
+    w[2, 40] = 7.9 * 2.0 ** 3   # in the E2M1 saturation region of its block
+    w[2, 41] = 1.0
+    w = w.numpy()
+    if fmt_name == "e4m3":
+        fmt, emax, signbit = orc.E4M3, 8, 0x80
+        grid = torch.arange(0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    else:
+        fmt, emax, signbit = orc.E2M1, 2, 0x8
+        grid = np.array(_golden()["e2m1_magnitudes"])
+    want_codes, want_scales = _brute_force_mx(w.astype(np.float64), grid, emax, signbit)
+    codes, scales = orc.quantize_f32(w, fmt)
+    assert np.array_equal(scales, want_scales)
+    if fmt == orc.E2M1:
+        assert codes.shape == (rows, K // 2)
+        codes = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(rows, K)
+    assert np.array_equal(codes, want_codes), np.argwhere(codes != want_codes)[:5]
+
+
+@pytest.mark.parametrize("fmt_name", ["e4m3", "e2m1"])
+def test_weight_quantiser_equals_row_quantiser(orc, fmt_name):
+    """quantize_f32 (fp32 input, rows split over threads) gives the same bytes
+    as quantize_rows on the same values widened to fp64, and rejects a
+    non-finite entry in any row."""
+    fmt = orc.E4M3 if fmt_name == "e4m3" else orc.E2M1
+    rows, K = 3 * (os.cpu_count() or 1) + 1, 160
+    w = (np.random.default_rng(5).standard_normal((rows, K)) * 0.02).astype(np.float32)
+    c32, s32 = orc.quantize_f32(w, fmt)
+    c64, s64 = orc.quantize_rows(w.astype(np.float64), fmt)
+    assert np.array_equal(c32, c64) and np.array_equal(s32, s64)
+    bad = w.copy()
+    bad[rows - 2, 7] = np.inf
+    with pytest.raises(ValueError):
+        orc.quantize_f32(bad, fmt)

@@ -51,6 +51,14 @@ MUTANTS = [
     ("e4m3_no_subnormal_binade", "int e = (a < ldexp(1.0, -6)) ? -6 : floor_log2(a);", "int e = floor_log2(a);"),
     ("negative_zero_loses_sign", "int sign = signbit(q) ? 0x80 : 0;", "int sign = (q < 0) ? 0x80 : 0;"),
     ("e2m1_packing_high_nibble_first", "if (col % 2 == 0) *p", "if (col % 2 == 1) *p"),
+    # weight quantisation (fp32 rows, split over threads)
+    ("f32_e2m1_row_stride_quarter", "int64_t row_bytes = (fmt == ORC_E4M3) ? K : K / 2;",
+     "int64_t row_bytes = (fmt == ORC_E4M3) ? K : K / 4;"),
+    ("f32_e4m3_row_stride_half", "int64_t row_bytes = (fmt == ORC_E4M3) ? K : K / 2;",
+     "int64_t row_bytes = (fmt == ORC_E4M3) ? K / 2 : K / 2;"),
+    ("f32_copies_row_0", "rowbuf[i] = (double)w[r * K + i];", "rowbuf[i] = (double)w[i];"),
+    ("f32_scales_of_row_0", "codes + r * row_bytes, scales + r * (K / 32)", "codes + r * row_bytes, scales"),
+    ("f32_status_dropped", "      if (rs) {\n#pragma omp atomic write\n        st = rs;\n      }\n", ""),
     # router
     ("topk_ties_to_highest_index", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] >= l[best])"),
     ("topk_ascending", "(best < 0 || l[e] > l[best])", "(best < 0 || l[e] < l[best])"),

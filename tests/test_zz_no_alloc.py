@@ -9,6 +9,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+
 pytestmark = pytest.mark.gpu
 
 
@@ -52,6 +54,40 @@ def test_no_alloc_permute_matches_workspace_permute(mx):
             got = _run(mx, lambda i, c, o, s: mx.moe_permute_no_alloc(i, E, c, o, s), ids, E)
             for a, b in zip(got, ref):
                 assert np.array_equal(a, b), (T, E, k)
+
+
+def _tied_ids(T, E, k, seed):
+    """Top-k of small-integer logits: many equal logits per token, so the ids
+    come from the lowest-index tie-break and many tokens share experts."""
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randint(-1, 2, (T, E), generator=g).float()
+    ids, _ = oracle.route_topk(logits.numpy(), k)
+    return torch.from_numpy(ids).cuda()
+
+
+def _same_as_workspace_form(mx, ids, E):
+    T, k = ids.shape
+    ws = mx.alloc_workspace(mx.moe_permute_workspace_size(T, E, k))
+    ref = _run(mx, lambda i, c, o, s: mx.moe_permute(i, E, c, o, s, ws), ids, E)
+    got = _run(mx, lambda i, c, o, s: mx.moe_permute_no_alloc(i, E, c, o, s), ids, E)
+    for a, b in zip(got, ref):
+        assert np.array_equal(a, b), (T, E, k)
+
+
+def test_no_alloc_permute_shape_changes_between_calls(mx):
+    """The shared array keeps the previous call's chunk tables and ranks: a
+    one-chunk call straight after a many-chunk call on another expert count,
+    and the reverse, must not see them."""
+    for T, E, k, seed in [(5000, 256, 6, 11), (40, 32, 4, 12), (7000, 96, 8, 13), (3, 512, 8, 14),
+                          (257, 8, 2, 15), (256, 64, 3, 16)]:
+        _same_as_workspace_form(mx, _ids(T, E, k, seed), E)
+
+
+def test_no_alloc_permute_ties(mx):
+    """Routing full of equal logits: many tokens per expert and ids that come
+    from the tie-break, one chunk and several chunks."""
+    for T, E, k, seed in [(200, 16, 4, 21), (3000, 64, 8, 22), (9, 8, 8, 23)]:
+        _same_as_workspace_form(mx, _tied_ids(T, E, k, seed), E)
 
 
 def test_no_alloc_permute_rejects_oversized_requests(mx):
