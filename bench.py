@@ -3,16 +3,19 @@
 
 One step = one pass of the whole layer (activation quantisation, top-k
 routing, permutation, grouped gate/up GEMM + SwiGLU + requant, grouped down
-GEMM + combine) over one batch of the synthetic workload, on one GPU.  The
-default workload is the decode MXFP8 layer (T=32, H=4096, I=1536, 128 experts
-top-8 + 1 shared).  Prints one JSON line (rank 0).
+GEMM + combine) over one batch of a synthetic workload, on one GPU.  The
+headline workload is the decode MXFP8 layer (T=32, H=4096, I=1536, 128 experts
+top-8 + 1 shared); the same run measures the other four layer shapes and puts
+them under "workloads" in the same JSON line (rank 0 prints one line).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--only] [--impl reference] [--no-cpu-baseline]
 
---impl reference times the CPU oracle (plain C, fp64) on a bounded sample of the
-same workload on this host's cores.  For N > 1 (torchrun) every rank runs an
-independent replica of the layer ("replicas only": the layer does not shard
-across GPUs here); throughput is the sum over ranks at the slowest rank's time.
+--impl reference times the CPU oracle (plain C, fp64) on the same workload,
+each step one oracle call on a batch of its tokens (the whole batch when K of
+them fit the time budget).  For N > 1 (torchrun) every rank runs an independent
+replica of the layer ("replicas only": the layer does not shard across GPUs
+here); throughput is the sum over ranks at the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -38,18 +41,25 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 MX8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
+METRIC = "MoE layer tokens/s"
+# the headline first, then the other layer shapes
+WORKLOAD_ORDER = ["decode_mxfp8", "tiny", "specverify_mxfp4", "decode_mxfp4", "prefill_mxfp8"]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_mxfp8", choices=list(W.WORKLOADS))
+    ap.add_argument("--only", action="store_true", help="measure the --workload shape alone")
     ap.add_argument("--impl", default="mxmoe", choices=["mxmoe", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
-    return ap.parse_args()
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0,
+                    help="oracle time per workload for the GPU arm's cpu_baseline")
+    ap.add_argument("--reference-budget-s", type=float, default=180.0,
+                    help="oracle time of the whole --impl reference run")
+    return ap.parse_args(argv)
 
 
 def dist_env():
@@ -73,6 +83,15 @@ def peaks():
         except Exception:
             pass
     return {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16s, "source": src}
+
+
+def config_of(wl: W.Workload, world: int) -> dict:
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k, "shared_experts": 1,
+            "weights": "MXFP8 E4M3" if wl.fmt == "e4m3" else "MXFP4 E2M1", "activations": "MXFP8 E4M3",
+            "router_bias": "1.1*ln(1/(e+1))" if wl.zipf_bias else "none",
+            "l2": "flushed between steps (2x L2 write outside the timed events)",
+            "parallelism": f"replicas x{world}"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -117,12 +136,13 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, window=None):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         lines = self.lines
-        if self.window is not None:
-            t0, t1 = self.window
+        window = window or self.window
+        if window is not None:
+            t0, t1 = window
             pad = 1.5 * self.PERIOD_MS * 1e-3
             inside = [ln for t, ln in lines if t0 <= t <= t1 + pad]
             lines = inside or [ln for t, ln in lines if t0 - pad <= t <= t1 + 2 * pad]
@@ -175,6 +195,14 @@ def weight_bytes_per_expert(wl: W.Workload):
     return w1, w2
 
 
+def gateup_algorithmic_bytes(wl: W.Workload, touched: int) -> float:
+    """Bytes the gate/up GEMM must move at least: the touched experts' W1 codes
+    and scales, each token's MXFP8 activation row once, h written once."""
+    w1b, _ = weight_bytes_per_expert(wl)
+    mx8 = 1.0 + 1.0 / 32
+    return touched * w1b + wl.T * wl.H * mx8 + wl.slots * wl.I * mx8
+
+
 def source_hash():
     """Hash of the code (comments and blank lines dropped) of the sources the
     dominant kernel and its launch schedule are built from."""
@@ -205,10 +233,14 @@ def ncu_traffic(kernel_tag: str, wl_name: str):
 
 
 # ------------------------------------------------------------------ CPU oracle timing
+_ORACLE_WEIGHTS = {}   # (H, I, E, fmt, seed, expert) -> oracle-quantised W1/W2 codes and scales
+
+
 class OracleRunner:
-    """The CPU oracle on bounded samples of a workload: each call evaluates a
-    few tokens of it (quantised weights of the experts those tokens touch are
-    drawn and quantised on first use, untimed)."""
+    """The CPU oracle on a workload: each call evaluates a batch of its tokens
+    (the experts those tokens touch are drawn and quantised by the oracle on
+    first use, untimed; workloads with the same weight shapes and format share
+    them)."""
 
     def __init__(self, wl: W.Workload):
         import oracle
@@ -223,28 +255,47 @@ class OracleRunner:
         self.next_token = 0
         self.threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
 
-    def call(self, n_tokens: int):
-        """Returns (tokens, seconds) of one timed oracle call."""
-        wl = self.wl
-        toks = sorted(set((self.next_token + i) % wl.T for i in range(n_tokens)))
-        self.next_token += n_tokens
-        for e in set(int(e) for e in self.ids[toks].ravel()) | {wl.E}:
-            if self.w[0][e] is None:
-                w1, w2 = W.draw_expert_weights(wl, e, 0, "cpu")
-                self.w[0][e], self.w[1][e] = self.oracle.quantize_f32(w1.numpy(), self.fmt)
-                self.w[2][e], self.w[3][e] = self.oracle.quantize_f32(w2.numpy(), self.fmt)
-        t0 = time.perf_counter()
-        self.oracle.moe_forward(self.x_bits, self.lg, wl.k, *self.w, self.fmt, wl.I, tokens=toks)
-        return len(toks), time.perf_counter() - t0
+    def tokens(self, n: int):
+        toks = sorted(set((self.next_token + i) % self.wl.T for i in range(n)))
+        self.next_token += n
+        return toks
 
-    def rate(self, budget_s: float, n_tokens: int = 2):
+    def prepare(self, toks):
+        wl = self.wl
+        for e in set(int(e) for e in self.ids[toks].ravel()) | {wl.E}:
+            if self.w[0][e] is not None:
+                continue
+            key = (wl.H, wl.I, wl.E, wl.fmt, 0, e)
+            if key not in _ORACLE_WEIGHTS:
+                w1, w2 = W.draw_expert_weights(wl, e, 0, "cpu")
+                _ORACLE_WEIGHTS[key] = (*self.oracle.quantize_f32(w1.numpy(), self.fmt),
+                                        *self.oracle.quantize_f32(w2.numpy(), self.fmt))
+            for i in range(4):
+                self.w[i][e] = _ORACLE_WEIGHTS[key][i]
+
+    def call(self, toks):
+        """Seconds of one oracle call on the token list `toks` (weights prepared first, untimed)."""
+        self.prepare(toks)
+        t0 = time.perf_counter()
+        self.oracle.moe_forward(self.x_bits, self.lg, self.wl.k, *self.w, self.fmt, self.wl.I,
+                                tokens=None if len(toks) == self.wl.T else toks)
+        return time.perf_counter() - t0
+
+    def baseline(self, budget_s: float, n_tokens: int, one_core: bool = False):
+        """cpu_baseline entry: oracle calls on batches of n_tokens until budget_s
+        of oracle time is spent (at least one call)."""
         done, spent, calls = 0, 0.0, 0
-        while spent < budget_s and calls < 256:
-            n, dt = self.call(n_tokens)
-            done, spent, calls = done + n, spent + dt, calls + 1
-        sample = (f"{done} tokens of the {self.wl.name} workload in {calls} oracle calls of {n_tokens} tokens "
-                  f"({spent:.1f} s; each call decodes the touched experts' weights to fp64 and runs fp64 GEMMs)")
-        return done / spent, sample
+        while calls == 0 or (spent < budget_s and calls < 64):
+            toks = self.tokens(n_tokens)
+            spent += self.call(toks)
+            done, calls = done + len(toks), calls + 1
+        what = "the whole batch" if n_tokens >= self.wl.T else f"{n_tokens} of its {self.wl.T} tokens"
+        sample = (f"{calls} oracle call(s), each on {what} of the {self.wl.name} workload "
+                  f"({done} tokens in {spent:.1f} s; each call decodes the touched experts' weights to fp64 "
+                  f"and runs fp64 loops)")
+        d = {"value": done / spent, "unit": "tokens/s", "cores": 1 if one_core else self.threads, "kind": "oracle",
+             "sample": sample}
+        return d
 
 
 # ------------------------------------------------------------------ replicas
@@ -264,27 +315,57 @@ def replica_throughput(world: int, T: int, ms: float) -> float:
     return world * T / (ms * 1e-3)
 
 
-# ------------------------------------------------------------------ main arms
+def cpu_sample_tokens(wl: W.Workload) -> int:
+    """Tokens per oracle call for the GPU arm's cpu_baseline: the whole batch,
+    except the 8192-token prefill (minutes of fp64 work), which takes a sample."""
+    return wl.T if wl.T <= 256 else 8
+
+
+# ------------------------------------------------------------------ reference arm
+def reference_plan(t_first: float, n_first: int, runner: OracleRunner, steps: int, budget_s: float):
+    """Tokens per step: the whole batch when `steps` whole-batch calls fit the
+    budget, else the largest batch whose estimated call time (the first call's
+    time scaled by the experts it touches) fits."""
+    wl = runner.wl
+    if steps * t_first <= budget_s:
+        return n_first
+    touched_full = len(set(int(e) for e in runner.ids[:n_first].ravel()) | {wl.E})
+    n = n_first
+    while n > 1:
+        n = max(1, n // 2)
+        touched = len(set(int(e) for e in runner.ids[:n].ravel()) | {wl.E})
+        if steps * t_first * touched / touched_full <= budget_s:
+            break
+    return n
+
+
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return
     runner = OracleRunner(wl)
-    per_step = []
-    for i in range(args.warmup + args.steps):
-        n, dt = runner.call(1)
-        if i >= args.warmup:
-            per_step.append(dt / n)
-    sec_per_token = float(np.mean(per_step))
-    rate = 1.0 / sec_per_token
-    sample = (f"each step: the oracle on 1 token of the {wl.name} workload (tokens taken in order), "
-              f"{args.steps} timed steps after {args.warmup} warm-up")
+    # the first warm-up step (untimed) is a call on the whole batch, or on the
+    # prefill sample: its time sizes the steps
+    n0 = cpu_sample_tokens(wl)
+    t_first = runner.call(list(range(n0)))
+    n_step = reference_plan(t_first, n0, runner, args.steps, args.reference_budget_s)
+    for _ in range(max(0, args.warmup - 1)):
+        runner.call(runner.tokens(n_step))
+    times, done = [], 0
+    for _ in range(args.steps):
+        toks = runner.tokens(n_step)
+        times.append(runner.call(toks))
+        done += len(toks)
+    spent = float(np.sum(times))
+    rate = done / spent
+    what = "the whole batch" if n_step >= wl.T else f"{n_step} of its {wl.T} tokens (taken in turn)"
+    sample = (f"each step one oracle call on {what} of the {wl.name} workload; "
+              f"{args.steps} timed steps after {args.warmup} warm-up, {spent:.1f} s of oracle time")
     line = {
-        "impl": "reference", "metric": "MoE layer tokens/s", "value": rate, "unit": "tokens/s",
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * sec_per_token * wl.T, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "shared_experts": 1, "weights": wl.fmt},
+        "ms_per_step": 1e3 * spent / args.steps, "tokens_per_step": n_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(wl, world),
         "cpu_baseline": {"value": rate, "unit": "tokens/s", "cores": runner.threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": rate, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -292,17 +373,11 @@ def run_reference(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_gpu(args, wl, rank, world, local):
-    from block_scaled_mx_gb300 import build as B
+# ------------------------------------------------------------------ GPU arm
+def measure_workload(args, wl, dev, world, clk, with_cpu):
+    """Times one workload; returns its entry (headline keys included)."""
     from block_scaled_mx_gb300 import mxmoe as mx
 
-    if rank == 0 or world == 1:
-        B.build()
-    if world > 1:
-        torch.distributed.barrier()
-        B.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
     layer, logits, x = build_gpu_layer(wl, dev)
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     fmt = layer.fmt
@@ -322,8 +397,6 @@ def run_gpu(args, wl, rank, world, local):
     out = torch.empty(T, H, dtype=torch.float32, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
-    nperm = 1 if T <= 256 else 2
 
     def step(ev):
         ev[0].record(stream)
@@ -345,14 +418,11 @@ def run_gpu(args, wl, rank, world, local):
         step(mk())
     torch.cuda.synchronize()
     if mx.moe_get_status(pws) or mx.moe_get_status(gws):
-        raise RuntimeError("device status error during warm-up")
+        raise RuntimeError(f"{wl.name}: device status error during warm-up")
     cnt = counts.cpu().numpy()
     touched = int(np.count_nonzero(cnt))
     w1b, w2b = weight_bytes_per_expert(wl)
     evs = [mk() for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     out_f = torch.empty(T, H, dtype=torch.float32, device=dev)
     fev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for _ in range(args.warmup):
@@ -382,31 +452,27 @@ def run_gpu(args, wl, rank, world, local):
         flush.fill_(1)
         run_fused()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        time.sleep(0.3)             # the sampler's first lines arrive before the timed region
-        t_wall0 = time.perf_counter()
-        for i in range(args.steps):
-            # (a) the layer through the fused single call: the step time
-            flush.fill_(1)          # L2 flush, outside the timed events
-            fev[i][0].record(stream)
-            run_fused()
-            fev[i][1].record(stream)
-            # (b) the same kernels through the step-wise calls, events between
-            #     them: per-kernel durations for the roofline
-            flush.fill_(1)
-            step(evs[i])
-        torch.cuda.synchronize()
-        t_wall1 = time.perf_counter()
-        t_wall = t_wall1 - t_wall0
-        clk.mark(t_wall0, t_wall1)
-        time.sleep(3 * ClockSampler.PERIOD_MS * 1e-3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        # (a) the layer through the fused single call: the step time
+        flush.fill_(1)          # L2 flush, outside the timed events
+        fev[i][0].record(stream)
+        run_fused()
+        fev[i][1].record(stream)
+        # (b) the same kernels through the step-wise calls, events between
+        #     them: per-kernel durations for the roofline
+        flush.fill_(1)
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
     if world > 1:
         torch.distributed.barrier()
     per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)] for i in range(args.steps)])
     fused_ms = np.array([a.elapsed_time(b) for a, b in fev])
-    ms = float(fused_ms.mean())
-    steps_ms = float(per.sum(1).mean())
-    ms = max_over_ranks(ms, world, dev)
+    ms = max_over_ranks(float(fused_ms.mean()), world, dev)
     value = replica_throughput(world, T, ms)
 
     # ---- e2e through the public single call with host buffers
@@ -436,82 +502,120 @@ def run_gpu(args, wl, rank, world, local):
         e2e_ms.append(e0.elapsed_time(e1))
     e2e = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
     if mx.moe_get_status(layer.workspace(T)):
-        raise RuntimeError("device status error in moe_forward")
+        raise RuntimeError(f"{wl.name}: device status error in moe_forward")
 
-    if rank != 0:
-        return
     pk = peaks()
     gemm1_ms = float(per[:, 3].mean())
     gemm2_ms = float(per[:, 4].mean())
-    # algorithmic bytes of the gate/up call: touched experts' W1 (codes + scales),
-    # the gathered activation rows read (and written once by the gather), h written
     slots = T * (k + 1)
-    act_bytes = slots * H * (1 + 1 / 32)
-    g1_bytes = touched * w1b + 2 * slots * H + slots * H / 32 + slots * I * (1 + 1 / 32)
-    g2_bytes = touched * w2b + act_bytes * 0 + slots * I * (1 + 1 / 32) + 2 * T * H * 4
     flops = 6.0 * slots * H * I
     tc_peak = pk["bf16_tflops"] * MX8_OVER_BF16
     hbm_peak = pk["hbm_gbs"]
     bw = touched * (w1b + w2b)
     layer_floor_ms = max(flops / (tc_peak * 1e12), bw / (hbm_peak * 1e9)) * 1e3
     dominant_hbm = flops / (tc_peak * 1e12) < bw / (hbm_peak * 1e9)
+    kname = "k_grouped_gemm (gate/up + SwiGLU + requant)"
     if dominant_hbm:
+        g1_bytes = gateup_algorithmic_bytes(wl, touched)
         achieved = g1_bytes / (gemm1_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": ncu_traffic("gemm1", wl.name), "kernel": "k_grouped_gemm (gate/up + SwiGLU + requant)",
-                "peak_source": pk["source"]}
+                "traffic": ncu_traffic("gemm1", wl.name), "kernel": kname, "algorithmic_bytes": g1_bytes,
+                "kernel_ms": gemm1_ms, "peak_source": pk["source"] + " copy bandwidth (burst)"}
     else:
         g1_flops = 4.0 * slots * H * I
         achieved = g1_flops / (gemm1_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": achieved / tc_peak, "traffic": ncu_traffic("gemm1", wl.name),
-                "kernel": "k_grouped_gemm (gate/up + SwiGLU + requant)",
-                "peak_source": pk["source"] + " bf16 x2 (nominal MXFP8/bf16 ratio)"}
-    cpu = None
-    if world == 1 and not args.no_cpu_baseline:
-        try:
-            runner = OracleRunner(wl)
-            rate, sample = runner.rate(args.cpu_budget_s * 2 / 3)
-            cpu = {"value": rate, "unit": "tokens/s", "cores": runner.threads, "kind": "oracle", "sample": sample}
-            if wl.T <= 64:  # small configurations: also one core, the oracle's per-core speed
-                try:
-                    runner.oracle.set_threads(1)
-                    rate1, sample1 = runner.rate(args.cpu_budget_s / 3, n_tokens=1)
-                finally:
-                    runner.oracle.set_threads(0)
-                cpu["value_1core"] = rate1
-                cpu["sample_1core"] = sample1
-        except Exception as exc:  # the GPU number stands without it
-            cpu = {"value": None, "unit": "tokens/s", "cores": None, "kind": "oracle", "sample": f"failed: {exc}"}
-    fused = T <= 256 and (T * (k + 1)) / (E + 1) < 48
-    fused_launches = 3 if fused else (1 + nperm + (1 if (T * (k + 1)) / (E + 1) >= 48 else 0) + 2)
-    wide = (T * (k + 1)) / (E + 1) >= 48
+                "frac": achieved / tc_peak, "traffic": ncu_traffic("gemm1", wl.name), "kernel": kname,
+                "algorithmic_flops": g1_flops, "kernel_ms": gemm1_ms,
+                "peak_source": pk["source"] + " bf16 burst x2 (nominal MXFP8/bf16 ratio)"}
+    fused_launches = mx.moe_forward_launches(T, H, I, E, k, fmt)
+    nperm = 1 if T <= 256 else 2
+    wide = fused_launches > 3 and (T * (k + 1)) / (E + 1) >= 48
     step_launches = 1 + 1 + nperm + (2 if wide else 1) + 1
-    line = {
-        "metric": "MoE layer tokens/s", "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "us_per_layer": ms * 1e3,
+    entry = {
+        "us_per_layer": ms * 1e3, "tokens_s": value, "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup,
         "launches_per_layer": fused_launches,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3" if wl.fmt == "e4m3" else "e2m1") + " x e4m3 -> f32 (MX block-scaled)",
-        "data": "synthetic",
-        "config": {"workload": wl.name, "T": T, "H": H, "I": I, "E": E, "k": k, "shared_experts": 1,
-                   "weights": "MXFP8 E4M3" if wl.fmt == "e4m3" else "MXFP4 E2M1",
-                   "activations": "MXFP8 E4M3", "l2": "flushed between steps (2x L2 write outside the timed events)",
-                   "timing": f"value: {fused_mode}; kernel times: the same kernels via the step-wise calls in the same loop",
-                   "parallelism": f"replicas x{world}", "sms": n_sm},
+        "timing": f"value: {fused_mode}; kernel times: the same kernels via the step-wise calls in the same loop",
         "roofline": roof,
         "layer_roofline": {"floor_us": layer_floor_ms * 1e3, "frac": layer_floor_ms / ms,
                            "touched_experts": touched, "weight_bytes": bw, "flops": flops,
                            "bound": "hbm" if dominant_hbm else "tensor"},
         "kernels_ms": {"quantize": float(per[:, 0].mean()), "topk": float(per[:, 1].mean()),
                        "permute+zero": float(per[:, 2].mean()), "gateup_call": gemm1_ms, "down_call": gemm2_ms,
-                       "step_calls_total": steps_ms},
+                       "step_calls_total": float(per.sum(1).mean())},
         "e2e": {"value": replica_throughput(world, T, e2e), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2 + T * E * 4,
                 "d2h_bytes_per_step": T * H * 4, "ms_per_step": e2e},
-        "cpu_baseline": cpu,
-        "clocks": clk.summary(),
+        "clocks": clk.summary((t_wall0, t_wall1)),
         "gpu_launches": (fused_launches + step_launches) * args.steps,
-        "wall_s_timed": t_wall,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    del layer, flush
+    torch.cuda.empty_cache()
+    if with_cpu:
+        entry["cpu_baseline"] = cpu_baseline(args, wl)
+    return entry
+
+
+def cpu_baseline(args, wl):
+    try:
+        runner = OracleRunner(wl)
+        cpu = runner.baseline(args.cpu_budget_s, cpu_sample_tokens(wl))
+        if wl.T <= 16:  # the smallest configurations: also one core, the oracle's per-core speed
+            try:
+                runner.oracle.set_threads(1)
+                one = runner.baseline(args.cpu_budget_s / 3, cpu_sample_tokens(wl), one_core=True)
+            finally:
+                runner.oracle.set_threads(0)
+            cpu["value_1core"] = one["value"]
+            cpu["sample_1core"] = one["sample"]
+        return cpu
+    except Exception as exc:  # the GPU number stands without it
+        return {"value": None, "unit": "tokens/s", "cores": None, "kind": "oracle", "sample": f"failed: {exc}"}
+
+
+def run_gpu(args, rank, world, local):
+    from block_scaled_mx_gb300 import build as B
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    if rank == 0 or world == 1:
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+        B.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    with_cpu = world == 1 and not args.no_cpu_baseline
+    names = [args.workload] + ([] if args.only else [n for n in WORKLOAD_ORDER if n != args.workload])
+    entries = {}
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)             # the sampler's first lines arrive before the first timed region
+        for n in names:
+            entries[n] = measure_workload(args, W.WORKLOADS[n], dev, world, clk, with_cpu and rank == 0)
+        time.sleep(3 * ClockSampler.PERIOD_MS * 1e-3)
+    if rank != 0:
+        return
+    head = entries.pop(args.workload)
+    wl = W.WORKLOADS[args.workload]
+    line = {
+        "metric": METRIC, "value": head["tokens_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "us_per_layer": head["us_per_layer"], "launches_per_layer": head["launches_per_layer"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3" if wl.fmt == "e4m3" else "e2m1") + " x e4m3 -> f32 (MX block-scaled)",
+        "data": "synthetic",
+        "config": config_of(wl, world),
+        "timing": head["timing"],
+        "roofline": head["roofline"],
+        "layer_roofline": head["layer_roofline"],
+        "kernels_ms": head["kernels_ms"],
+        "e2e": head["e2e"],
+        "cpu_baseline": head.get("cpu_baseline"),
+        "clocks": head["clocks"],
+        "gpu_launches": head["gpu_launches"],
+        "wall_s_timed": head["wall_s_timed"],
+        "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
+        "build": {"stamp": mx.mx_build_stamp(), "compiled_in_this_run": bool(B.LAST_BUILD.get("compiled"))},
+        "workloads": {n: dict(e, config=config_of(W.WORKLOADS[n], world)) for n, e in entries.items()},
     }
     print(json.dumps(line), flush=True)
 
@@ -526,7 +630,7 @@ def main():
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     try:
-        run_gpu(args, wl, rank, world, local)
+        run_gpu(args, rank, world, local)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -60,6 +60,17 @@ size_t gather_bytes(int T, int H, int E, int k) {
   return wide_schedule(T, E, k) ? al256(static_cast<size_t>(T) * (k + 1) * H) : 0;
 }
 
+// Kernel launches moe_forward enqueues for a shape (mirrors its branches):
+// the prologue; the chunked permutation when the prologue cannot permute
+// (count + scatter, or count alone for one chunk); the row gather of the wide
+// schedule; the two grouped GEMMs.
+int forward_launches(int T, int E, int k) {
+  const bool wide = wide_schedule(T, E, k);
+  const bool fused = T <= kPermuteChunk && !wide;
+  const int nchunks = (T + kPermuteChunk - 1) / kPermuteChunk;
+  return 1 + (fused ? 0 : (nchunks > 1 ? 2 : 1)) + (wide ? 1 : 0) + 2;
+}
+
 // moe_forward workspace carve (status word first, shared with the permutation
 // scratch).
 struct ForwardWs {
@@ -345,6 +356,12 @@ int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, co
                    k, out, f.perm.status, s, 2);
 }
 
+int moe_forward_launches(int T, int H, int I, int E, int k, int fmt) {
+  if (check_gemm_shape(T, H, I, E, k, fmt) != MX_OK) return -1;
+  if (T == 0) return 0;
+  return forward_launches(T, E, k);
+}
+
 int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {
   if (!ws || !host_status) return MX_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -357,5 +374,10 @@ int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {
 }
 
 void mx_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
+
+#ifndef MXMOE_BUILD_STAMP
+#define MXMOE_BUILD_STAMP "unstamped"
+#endif
+const char* mx_build_stamp(void) { return MXMOE_BUILD_STAMP; }
 
 }  // extern "C"

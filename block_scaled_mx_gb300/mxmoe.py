@@ -46,8 +46,10 @@ SIGNATURES = {
     "moe_grouped_gemm_down_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_forward_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_get_status": (_I, [_P, _P, _P]),
     "mx_debug_set_wait_limit_ns": (None, [_U64]),
+    "mx_build_stamp": (ctypes.c_char_p, []),
 }
 
 _lib = None
@@ -191,6 +193,11 @@ def moe_forward(x, logits, w1_prep, w2_prep, fmt, I, k, out, ws, stream=None):
                              _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_forward")
 
 
+def moe_forward_launches(T, H, I, E, k, fmt) -> int:
+    """Kernel launches moe_forward enqueues for this shape (host only)."""
+    return lib().moe_forward_launches(T, H, I, E, k, _fmt(fmt))
+
+
 def moe_get_status(ws, stream=None) -> int:
     v = ctypes.c_int(0)
     _check(lib().moe_get_status(_ptr(ws), _stream(stream), ctypes.addressof(v)), "moe_get_status")
@@ -199,6 +206,11 @@ def moe_get_status(ws, stream=None) -> int:
 
 def mx_debug_set_wait_limit_ns(ns: int):
     lib().mx_debug_set_wait_limit_ns(int(ns))
+
+
+def mx_build_stamp() -> str:
+    """Hash of the sources and flags the loaded library was compiled from."""
+    return lib().mx_build_stamp().decode()
 
 
 # ------------------------------------------------------------------ buffers (caller-owned memory)

@@ -83,7 +83,10 @@ MX_API const char* mx_status_string(int status);
  * even and saturated to +-448; a negative value that rounds to zero keeps its
  * sign (0x80).  Bit-exact with the reference definition.
  * Errors: MX_ERR_INVALID_ARG (null, T < 0, H <= 0), MX_ERR_UNSUPPORTED
- * (H % 32), MX_ERR_ALIGNMENT (x or codes not 16-byte aligned). */
+ * (H % 32), MX_ERR_ALIGNMENT (x or codes not 16-byte aligned).
+ * Source: the MI355X page (opening results list: MXFP8 and MXFP4 models;
+ * the passage on the native MXFP8 linear backend); the element and scale rule
+ * is that of OCP MX v1.0. */
 MX_API int mx_quantize_act(const void* x_bf16, int T, int H, uint8_t* codes, uint8_t* scales,
                     mx_stream_t stream);
 
@@ -99,7 +102,12 @@ MX_API int mx_quantize_weights(const float* w, int64_t rows, int K, int fmt, uin
  *   logits [T, E] fp32; topk_ids [T, k] int32; topk_w [T, k] fp32.
  * Ids are bit-exact with the reference; weights are fp32 (a few ulp).
  * Errors: MX_ERR_INVALID_ARG (null, T < 0, E <= 0, k < 1, k > E, k > 32),
- * MX_ERR_UNSUPPORTED (E > 1024). */
+ * MX_ERR_UNSUPPORTED (E > 1024).
+ * Source: the MI355X page, Figure 4 and its passage (each token's routed
+ * experts, with the shared expert added as a slot every token selects) and the
+ * correctness passage (the expert mask a token is routed through must be
+ * exact); the Kimi K3 page, section on the MXFP4 top-k finalize.  The pages fix
+ * no tie rule: lowest index first is this library's reading. */
 MX_API int moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                    mx_stream_t stream);
 
@@ -115,7 +123,13 @@ MX_API size_t moe_permute_workspace_size(int T, int E, int k);
  * topk_ids must hold k distinct ids in [0, E) per token; an id out of range
  * sets MX_ERR_DEVICE_ARG in the workspace status and is skipped.
  * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (E > 1024),
- * MX_ERR_WORKSPACE (ws_bytes < moe_permute_workspace_size). */
+ * MX_ERR_WORKSPACE (ws_bytes < moe_permute_workspace_size).
+ * Source: the MI355X page, Figure 3 and its passage (the routed token count of
+ * each expert is that expert's local M; grouped MoE programs are ordered so
+ * that neighbours reuse activation rows and expert weight tiles) and Figure 4
+ * (the shared expert sits in the routed table and the grouped GEMMs process it
+ * in the same pass).  Expert-major, token-ascending order is this library's
+ * reading, chosen so the result is unique. */
 MX_API int moe_permute(const int32_t* topk_ids, int T, int E, int k, int32_t* counts, int32_t* offsets,
                 int32_t* sorted_slot, void* ws, size_t ws_bytes, mx_stream_t stream);
 
@@ -150,7 +164,9 @@ MX_API size_t moe_prepared_weight_bytes(int E1, int H, int I, int fmt, int which
  *   rows/K = 2I/H for which = 1 and H/I for which = 2.
  *   dst: moe_prepared_weight_bytes(...) bytes, 256-byte aligned.
  * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H or I not a multiple of
- * 128), MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE (dst_bytes too small). */
+ * 128), MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE (dst_bytes too small).
+ * Source: the MI355X page, the passage after Figure 4 (MXFP8 weight and scale
+ * re-layout moved to model load; serving uses the prepared form directly). */
 MX_API int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E1, int H, int I, int fmt,
                         int which, void* dst, size_t dst_bytes, mx_stream_t stream);
 
@@ -169,7 +185,11 @@ MX_API size_t moe_gemm_workspace_size(int T, int H, int I, int E, int k);
  * fp32 accumulation means an h code next to a rounding boundary may differ by
  * one step from an exact-arithmetic reference.
  * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H or I % 128, E > 1024),
- * MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE, MX_ERR_CUDA. */
+ * MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE, MX_ERR_CUDA.
+ * Source: the MI355X page, Figure 3 and its passage (separate small-M and
+ * large-M launchers, tiles chosen from the local shape, grouped programs
+ * reordered for cache reuse), Figure 4 (routed and shared experts in one
+ * grouped GEMM) and the correctness passage (packed gate/up slices, SwiGLU). */
 MX_API int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
                             const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
                             int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
@@ -179,7 +199,11 @@ MX_API int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_
  *   out[t, :] += w_s * sum_i h[p,i] Wd[e,:,i]   (w_s = topk_w[t,j] for a routed
  *   slot, 1 for the shared slot), fp32 atomic adds into `out`.
  *   out [T, H] fp32 must be zero-filled (or hold a residual) by the caller.
- * Errors: as moe_grouped_gemm_swiglu. */
+ * Errors: as moe_grouped_gemm_swiglu.
+ * Source: the Kimi K3 page, section on moving the MXFP4 top-k finalize into
+ * the epilogue (one launch and one intermediate write/read removed); the
+ * MI355X page, Figure 4 (the shared expert's output added with the routed
+ * ones). */
 MX_API int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
                                   const int32_t* offsets, const int32_t* sorted_slot,
                                   const float* topk_w, const void* w2_prep, int fmt, int T, int H,
@@ -191,10 +215,18 @@ MX_API size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt);
 
 /* The whole layer in one call, no host synchronisation: quantise, route,
  * permute, both grouped GEMMs; out [T, H] fp32 is overwritten.
- * Errors: union of the step calls. */
+ * Errors: union of the step calls.
+ * Source: the MI355X page, the passage on launch cost and graph execution and
+ * Figure 4's passage (removing launches and intermediate traffic raised output
+ * throughput most at concurrency 1); the Ling-3.0-flash page, on kernel nodes
+ * of 1.5-6 us each whose launch floor is comparable to their arithmetic. */
 MX_API int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
                 int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                 mx_stream_t stream);
+
+/* Number of kernel launches moe_forward enqueues for this shape (host only;
+ * -1 for a shape moe_forward rejects, 0 for T = 0). */
+MX_API int moe_forward_launches(int T, int H, int I, int E, int k, int fmt);
 
 /* Copy the workspace status word to *host_status (synchronising `stream`) and
  * clear it.  0 = no device-side error; otherwise an MX_ERR_* code. */
@@ -204,6 +236,11 @@ MX_API int moe_get_status(void* ws, mx_stream_t stream, int* host_status);
  * the GEMM kernels (default 2e9).  A tiny limit makes the waits run out, which
  * exercises the MX_ERR_TIMEOUT path without hanging the GPU. */
 MX_API void mx_debug_set_wait_limit_ns(uint64_t ns);
+
+/* Hash of the sources, flags and compiler this library was built from
+ * (16 hex digits; static string).  Lets a caller check that the library it
+ * loaded was compiled from the sources it expects. */
+MX_API const char* mx_build_stamp(void);
 
 #ifdef __cplusplus
 }

@@ -106,3 +106,22 @@ def test_binding_refuses_host_and_strided_tensors(L):
     with pytest.raises(ValueError, match="contiguous"):
         mx._ptr(meta)
     assert mx._ptr(None) is None and mx._ptr(4096) == 4096
+
+
+def test_loaded_library_is_built_from_these_sources(L):
+    """The stamp compiled into the library equals the hash of the current
+    sources, headers, flags and compiler (a stale or foreign build is rebuilt)."""
+    from block_scaled_mx_gb300 import build as B
+
+    assert L.mx_build_stamp().decode() == B.source_stamp() == B.built_stamp()
+
+
+def test_forward_launch_count(L):
+    """moe_forward's launch count is a host-side answer: three at decode sizes
+    (prologue with the permutation, two grouped GEMMs), -1 for rejected shapes,
+    0 for no tokens."""
+    assert L.moe_forward_launches(32, 4096, 1536, 128, 8, 0) == 3
+    assert L.moe_forward_launches(6, 2048, 512, 512, 8, 1) == 3
+    assert L.moe_forward_launches(0, 256, 128, 8, 2, 0) == 0
+    assert L.moe_forward_launches(16, 256, 100, 8, 2, 0) == -1
+    assert L.moe_forward_launches(8192, 4096, 1536, 128, 8, 0) >= 3

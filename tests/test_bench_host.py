@@ -86,3 +86,54 @@ def test_weight_bytes_per_expert_include_the_scales():
     wl4 = W.WORKLOADS["decode_mxfp4"]
     w1, w2 = bench.weight_bytes_per_expert(wl4)
     assert w1 + w2 == 3 * wl4.H * wl4.I * (0.5 + 1 / 32) == 10_027_008  # MXFP4: 0.53125 B per element
+
+
+def test_gateup_algorithmic_bytes():
+    """Touched experts' W1 (codes + scales), each activation row once, h once."""
+    wl = W.WORKLOADS["decode_mxfp8"]
+    w1, _ = bench.weight_bytes_per_expert(wl)
+    got = bench.gateup_algorithmic_bytes(wl, 113)
+    assert got == 113 * w1 + 32 * 4096 * 1.03125 + 32 * 9 * 1536 * 1.03125
+
+
+def test_both_arms_describe_the_workload_alike():
+    for name, wl in W.WORKLOADS.items():
+        a, b = bench.config_of(wl, 1), bench.config_of(W.WORKLOADS[name], 1)
+        assert a == b and a["workload"] == name and a["T"] == wl.T
+    assert bench.config_of(W.WORKLOADS["prefill_mxfp8"], 1)["router_bias"] != "none"
+
+
+class _Runner:
+    def __init__(self, wl, ids):
+        self.wl, self.ids = wl, ids
+
+
+def test_reference_plan_keeps_the_whole_batch_when_it_fits():
+    import numpy as np
+
+    wl = W.WORKLOADS["decode_mxfp8"]
+    rng = np.random.default_rng(0)
+    ids = np.stack([rng.choice(wl.E, wl.k, replace=False) for _ in range(wl.T)])
+    r = _Runner(wl, ids)
+    assert bench.reference_plan(1.0, wl.T, r, steps=20, budget_s=180) == wl.T
+    n = bench.reference_plan(11.0, wl.T, r, steps=100, budget_s=180)
+    assert 1 <= n < wl.T
+    touched = len(set(ids[:n].ravel().tolist()) | {wl.E})
+    touched_full = len(set(ids.ravel().tolist()) | {wl.E})
+    assert 100 * 11.0 * touched / touched_full <= 180 or n == 1
+
+
+def test_reference_arm_line(tmp_path):
+    """The reference arm on the tiny workload: same config as the GPU arm, every
+    step one whole-batch oracle call, ms_per_step x steps = oracle time spent."""
+    import subprocess
+
+    p = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "3",
+                        "--warmup", "2"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    line = json.loads([l for l in p.stdout.splitlines() if l.startswith("{")][-1])
+    assert line["config"] == bench.config_of(W.WORKLOADS["tiny"], 1)
+    assert line["tokens_per_step"] == 16 and line["steps"] == 3
+    spent = float(line["cpu_baseline"]["sample"].split(" s of oracle time")[0].split()[-1])
+    assert abs(line["ms_per_step"] * 3 / 1e3 - spent) <= 0.05 + 0.01 * spent
+    assert abs(line["value"] - 3 * 16 / (line["ms_per_step"] * 3 / 1e3)) <= 1e-6 * line["value"]

@@ -150,8 +150,29 @@ def _steps(L):
     return r
 
 
+def _signed_code_index(c):
+    """E4M3 code -> signed position on the value grid (+0 and -0 both 0):
+    magnitudes grow with the low seven bits, so neighbours differ by one."""
+    c = c.astype(np.int64)
+    return np.where(c & 0x80, -(c & 0x7F), c & 0x7F)
+
+
+def _e4m3_quantum(v, scale_codes):
+    """Spacing of the E4M3 grid at |v| under the block scale 2^(code - 127):
+    2^(e - 3) in the binade 2^e of |v| / scale, 2^-9 below 2^-6."""
+    S = np.exp2(scale_codes.astype(np.float64) - 127)
+    a = np.maximum(np.abs(v) / S, 2.0 ** -6)
+    _, ex = np.frexp(a)
+    return S * np.exp2(ex - 1 - 3)
+
+
 def _check_h(r, ref, I):
-    """h codes: GPU rows are slot positions, oracle rows are slot ids."""
+    """h codes against the oracle (GPU rows are slot positions, oracle rows are
+    slot ids).  fp32 tensor-core accumulation can move a value across an E4M3
+    rounding boundary (one code step), or move a block's amax across a power of
+    two (the block's scale moves by one and its codes re-round): every mismatch
+    must be one of those.  Returns (mismatch fraction, relative L2 of the
+    decoded h)."""
     ss = r["ss"].cpu().numpy()
     gc = r["h_c"].cpu().numpy()
     gs = r["h_s"].cpu().numpy()
@@ -159,6 +180,16 @@ def _check_h(r, ref, I):
     rs = ref["h_scales"][ss]
     gv = oracle.decode_matrix(gc, gs, oracle.E4M3)
     rv = oracle.decode_matrix(rc, rs, oracle.E4M3)
+    gs_e = np.repeat(gs, 32, axis=1)
+    rs_e = np.repeat(rs, 32, axis=1)
+    same_scale = gs_e == rs_e
+    assert np.all(np.abs(gs.astype(np.int64) - rs.astype(np.int64)) <= 1), "a block scale moved by more than one"
+    step = np.abs(_signed_code_index(gc) - _signed_code_index(rc))
+    assert np.all(step[same_scale] <= 1), "a code moved by more than one step under the same scale"
+    coarse = np.maximum(gs_e, rs_e)
+    moved = ~same_scale
+    tol = _e4m3_quantum(np.maximum(np.abs(gv), np.abs(rv))[moved], coarse[moved])
+    assert np.all(np.abs(gv - rv)[moved] <= tol), "a re-scaled value moved by more than one step of the coarser scale"
     frac = np.count_nonzero(gc != rc) / gc.size
     rel = np.linalg.norm(gv - rv) / np.linalg.norm(rv)
     return frac, rel
@@ -206,7 +237,8 @@ def test_layer_parity(name):
     assert np.array_equal(r["offsets"].cpu().numpy(), ro)
     assert np.array_equal(r["ss"].cpu().numpy(), rs)
     frac, hrel = _check_h(r, ref, wl.I)
-    assert frac < 0.02 and hrel < 0.02, (frac, hrel)
+    print(f"h codes {name}: mismatch fraction {frac:.2e}, decoded rel L2 {hrel:.2e}")
+    assert frac < 0.005 and hrel < 0.01, (frac, hrel)
     rel, mabs = out_errors(r["out"].double().cpu().numpy(), ref["out"])
     assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
     # the fused single call gives the same layer
