@@ -51,6 +51,14 @@ int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
   return MX_OK;
 }
 
+// The wide schedule runs the grouped GEMMs as CTA pairs (M = 256 MMAs over two
+// SMs, each loading half of a tile's token rows) when every pair tile has its
+// full four weight row blocks; MXMOE_PAIR=0 turns that off (A/B runs).
+void choose_pair(GemmArgs& a) {
+  const char* env = std::getenv("MXMOE_PAIR");
+  a.pair = (!a.gather4 && !(env && env[0] == '0') && pair_supported(a)) ? 1 : 0;
+}
+
 // The narrow schedule gathers each tile's few token rows with TMA gather4; the
 // wide schedule first copies the activation rows into slot order (one row-gather
 // kernel) so that each stage's 128 token rows arrive as one TMA box.
@@ -145,6 +153,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.h_scales = h_scales;
   a.status = status;
   a.wait_limit_ns = g_wait_limit_ns;
+  choose_pair(a);
   return cuda_status(launch_grouped_gemm(a, s));
 }
 
@@ -173,6 +182,7 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.pdl = pdl;
   a.bn = choose_bn(T, E, k, 1);
   a.wait_limit_ns = g_wait_limit_ns;
+  choose_pair(a);
   return cuda_status(launch_grouped_gemm(a, s));
 }
 

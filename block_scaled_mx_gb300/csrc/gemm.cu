@@ -64,8 +64,10 @@ struct GemmParams {
   int K, NK, NM, RB;
   int MG;  // weight tiles per tile group: groups of MG weight tiles (of every expert and
            // token tile) run one after the other, so the down GEMM's combine targets
-           // one slice of `out` at a time (L2-resident atomics)
+           // one slice of `out` at a time (L2-resident atomics).  With a CTA pair,
+           // NM and MG count pair tiles (two weight tiles each).
   int bn, stages, acc_bufs;
+  int brows;  // token rows one B box loads: bn, or bn / 2 per CTA of a pair
   int n_rows;
   uint32_t a_tx;
   const uint8_t* w_scales;
@@ -99,7 +101,9 @@ struct Shared {
   uint64_t* acc_full;
   uint64_t* acc_empty;
   uint64_t* drain;
+  uint64_t* exit_bar;  // CTA pair: the peer has finished every role
   uint32_t* tmem_slot;
+  uint32_t rank;       // rank in the CTA pair (0 without one)
 };
 
 // Tile t -> (group, expert, token tile, weight tile).  Tiles are ordered group-
@@ -126,22 +130,34 @@ __device__ __forceinline__ Tile decode_tile(int t, const Shared& sh, int E, int 
   return tl;
 }
 
+// Abort every role of this CTA (and of the peer CTA of a pair).
+template <bool PAIR>
+__device__ __forceinline__ void set_abort(const Shared& sh) {
+  *sh.abort_flag = 1;
+  if (PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(sh.abort_flag)), sh.rank ^ 1u), 1u);
+}
+
 // Wait that also gives up when another role has aborted.
 // SLEEP: poll with a suspend-time hint (whole warps that wait long); the
 // single MMA-issuing thread polls without one, to resume the moment a stage
-// lands.
-template <bool SLEEP = true>
+// lands.  PAIR: the barrier also receives arrivals from the peer CTA
+// (cluster-scope acquire).
+template <bool PAIR, bool SLEEP = true>
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
                                          unsigned long long limit_ns, int* status) {
   const uint32_t b = smem_u32(bar);
-  if (mbar_try_wait(b, parity)) return true;
+  auto poll = [&](bool sleep) {
+    if (PAIR) return sleep ? mbar_try_wait_cluster_sleep(b, parity, 20000u) : mbar_try_wait_cluster(b, parity);
+    return sleep ? mbar_try_wait_sleep(b, parity, 20000u) : mbar_try_wait(b, parity);
+  };
+  if (poll(false)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (SLEEP ? mbar_try_wait_sleep(b, parity, 20000u) : mbar_try_wait(b, parity)) return true;
+    if (poll(SLEEP)) return true;
     if (*sh.abort_flag) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
       set_status(status, MX_ERR_TIMEOUT);
-      *sh.abort_flag = 1;
+      set_abort<PAIR>(sh);
       return false;
     }
   }
@@ -149,28 +165,53 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32
 
 // Whole-warp form of wait_bar: every lane polls, and the outcome is made
 // uniform so that the warp leaves (or continues) together.
+template <bool PAIR>
 __device__ __forceinline__ bool warp_wait_bar(const Shared& sh, uint64_t* bar, uint32_t parity,
                                               unsigned long long limit_ns, int* status) {
-  const bool ok = wait_bar(sh, bar, parity, limit_ns, status);
+  const bool ok = wait_bar<PAIR>(sh, bar, parity, limit_ns, status);
   return __all_sync(0xffffffffu, ok) != 0;
+}
+
+// Arrive on a barrier of the pair's rank-0 CTA (this CTA's own without a pair).
+template <bool PAIR>
+__device__ __forceinline__ void arrive_leader(const Shared& sh, uint64_t* bar) {
+  if (PAIR) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0u));
+  else mbar_arrive(smem_u32(bar));
 }
 
 // One 128-wide K chunk of a tile: four K = 32 steps, each an MMA per row
 // block (gate and up, or two row blocks of W2) into its own accumulator;
 // `accum` turns on after the tile's first step.
-template <bool TWO>
+template <bool PAIR, bool TWO>
 __device__ __forceinline__ void issue_chunk(uint32_t d0, uint32_t d1, uint32_t a_lo, uint32_t b_lo, uint32_t sf,
                                             const uint32_t (&idesc)[4], uint32_t& accum) {
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
-    mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
-    if (TWO)
-      mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
-                      sf + 16u, accum);
+    if (PAIR) {
+      mma_mxf8f6f4_pair_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
+      if (TWO)
+        mma_mxf8f6f4_pair_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
+                             sf + 16u, accum);
+    } else {
+      mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
+      if (TWO)
+        mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
+                        sf + 16u, accum);
+    }
     accum = 1u;
   }
 }
 
+// PAIR: the kernel runs as clusters of two CTAs on neighbouring SMs.  A work
+// unit is (expert, token tile, pair of weight tiles); rank r takes weight tile
+// 2u + r of the unit's pair and half r of its token rows, and rank 0 issues
+// M = 256 MMAs that use both CTAs' operands and write both CTAs' accumulators
+// (the token rows each SM loads are halved against one CTA per tile).  The
+// pipeline's full barriers and the accumulator-free barriers live in rank 0
+// (rank 1's TMA loads, scale-staging and epilogue warps arrive on them
+// remotely); the MMA commits free the stage and signal the accumulator in both
+// CTAs at once.
+template <bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
@@ -190,8 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.acc_full = bars + 2 * S;
   sh.acc_empty = bars + 2 * S + 2;
   sh.drain = bars + 2 * S + 4;
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
-  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 6);
+  sh.exit_bar = bars + 2 * S + 5;
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 7);
+  sh.rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = sh.rank == 0;
+  // work units: one per CTA, or one per CTA pair
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_step = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   // ---- set-up that needs nothing from the previous grid (barriers, tensor
   // memory) runs before waiting on it; then the expert offsets, per-expert
@@ -200,22 +247,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // a stage is full when its TMA bytes have landed (producer: 1 arrival
-      // with the byte count) and the four scale-staging warps have put its
-      // scale factors into tensor memory (4 arrivals)
-      mbar_init(smem_u32(&sh.full[s]), 5);
+      // with the byte count; a pair's rank 0 counts both CTAs' bytes) and the
+      // scale-staging warps have put its scale factors into tensor memory (4
+      // arrivals per CTA)
+      mbar_init(smem_u32(&sh.full[s]), PAIR ? 9 : 5);
       mbar_init(smem_u32(&sh.empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.acc_full[a]), 1);
-      mbar_init(smem_u32(&sh.acc_empty[a]), kEpiWarps);
+      mbar_init(smem_u32(&sh.acc_empty[a]), PAIR ? 2 * kEpiWarps : kEpiWarps);
     }
     mbar_init(smem_u32(sh.drain), 1);
+    mbar_init(smem_u32(sh.exit_bar), 1);
     *sh.abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
-    tmem_alloc(smem_u32(sh.tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(smem_u32(sh.tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(sh.tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (p.pdl == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   if (p.pdl != 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -251,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // a pair's barriers must be initialised before the peer arrives on them
+  if (PAIR) cluster_sync_all();
   tc_fence_after();
   const uint32_t tbase = *sh.tmem_slot;
   const int per_group = sh.prefix[E1];
@@ -278,8 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t it = 0, rs = 0, rph = 0;
     bool ok = true;
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
+      // a pair's MMA takes token rows [0, N/2) from rank 0 and [N/2, N) from
+      // rank 1, N the tile's rows rounded up to 16
+      int n_mma = (tl.rows + 15) & ~15;
+      if (n_mma < 16) n_mma = 16;
+      const int b_row0 = tl.p0 + (PAIR ? static_cast<int>(sh.rank) * (n_mma >> 1) : 0);
       // the tile's two row blocks are prepared blocks 2m and 2m + 1 of each K
       // chunk (gate and up block m in W1): one TMA box
       // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token)
@@ -294,25 +356,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok[j] = (tt < 0 || tt >= p.T) ? 0 : tt;
         }
       }
-      const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.bn) * 128u;
+      const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.brows) * 128u;
       const uint32_t bytes = (2u * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
-        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
+        if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
         }
-        const uint32_t full = smem_u32(&sh.full[s]);
+        const uint32_t full = PAIR ? mapa_shared(smem_u32(&sh.full[s]), 0u) : smem_u32(&sh.full[s]);
         const uint32_t su = s * static_cast<uint32_t>(kps);  // first chunk slot
         if (lane == 0) {
-          mbar_arrive_expect_tx(full, bytes);
+          if (!PAIR) mbar_arrive_expect_tx(full, bytes);
+          else if (leader) mbar_arrive_expect_tx_cluster(full, 2u * bytes);   // both CTAs' loads
           for (int u = 0; u < kps; ++u) {
             const int kc = ks + u;
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
             // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
             // the TMA fills zeros and still counts the whole box)
-            const int blk0 = (tl.e * NK + kc) * p.RB + 2 * tl.m;
-            tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
+            const int blk0 = (tl.e * NK + kc) * p.RB + 2 * m;
+            if (PAIR) tma_load_3d_pair(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
+            else tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
           }
         }
         if (!b_ready) {
@@ -321,8 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int u = 0; u < kps; ++u) {
           const int kc = ks + u;
-          const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.bn * 128u);
-          if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, tl.p0, full);
+          const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.brows * 128u);
+          if (lane == 0 && !gather) {
+            if (PAIR) tma_load_2d_pair(b_s, &tm_b, kc * 128, b_row0, full);
+            else tma_load_2d(b_s, &tm_b, kc * 128, b_row0, full);
+          }
           __syncwarp();
           if (gather && lane < n4)
             tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
@@ -335,8 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // drain: every fill this warp armed has landed before the CTA exits
-    if (lane == 0) {
+    // drain: every fill this warp armed has landed before the CTA exits (a
+    // pair's rank 0 counts both CTAs' loads on its full barriers; rank 1 is
+    // held at the exit handshake until rank 0 has drained)
+    if (lane == 0 && (!PAIR || leader)) {
       const uint32_t n_fills = it;
       for (int s = 0; s < S && static_cast<uint32_t>(s) < n_fills; ++s) {
         const uint32_t last = n_fills - 1 - ((n_fills - 1 - s) % S);
@@ -345,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && (!PAIR || leader)) {
       // everything the issue loop needs lives in registers, and the ring and
       // accumulator positions advance incrementally: the single issuing thread's
       // per-stage latency (divisions, parameter reloads) is MMA issue time lost
@@ -359,24 +428,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sf_base = tbase + p.sf_col0;
       const uint32_t a_base = smem_u32(base + p.off_a);
       const uint32_t b_base = smem_u32(base + p.off_b);
-      const uint32_t b_stride16 = static_cast<uint32_t>(p.bn) * (128u >> 4);
+      const uint32_t b_stride16 = static_cast<uint32_t>(p.brows) * (128u >> 4);
       const uint32_t kps = static_cast<uint32_t>(p.kps);
       // descriptors of slot 0 (start address field is addr >> 4; slots add to it)
       const uint32_t a_lo0 = desc_lo_sw128(a_base);
       const uint32_t b_lo0 = desc_lo_sw128(b_base);
+      constexpr uint32_t kM = PAIR ? 256u : 128u;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit0; t < total && ok; t += unit_step) {
         const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
-        const bool two = p.epi == 0 || (2 * tl.m + 1 < p.RB);
+        const int m = PAIR ? 2 * tl.m : tl.m;   // a pair's tiles both have two row blocks
+        const bool two = p.epi == 0 || (2 * m + 1 < p.RB);
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
-        if (!wait_bar(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
+        if (!wait_bar<PAIR>(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
         tc_fence_after();
         const uint32_t d0 = tbase + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
         const uint32_t d1 = tbase + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
         uint32_t idesc[4];
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, 128, n_mma, kb, kb);
+        for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, kM, n_mma, kb, kb);
         uint32_t accum = 0u;
         for (int ks = 0; ks < NKs; ++ks) {
           const uint32_t s = rs, ph = rph;
@@ -384,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs = 0;
             rph ^= 1u;
           }
-          if (!wait_bar<false>(sh, &sh.full[s], ph, lim, status)) {
+          if (!wait_bar<PAIR, false>(sh, &sh.full[s], ph, lim, status)) {
             ok = false;
             break;
           }
@@ -394,40 +465,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           // is tensor time
           const uint32_t slot0 = s * kps;
           if (two) {
-            issue_chunk<true>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
-                              sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            issue_chunk<PAIR, true>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
+                                    sf_base + slot0 * kSfColsPerChunk, idesc, accum);
             if (kps == 2)
-              issue_chunk<true>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
-                                sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
+              issue_chunk<PAIR, true>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
+                                      sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
           } else {
-            issue_chunk<false>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
-                               sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            issue_chunk<PAIR, false>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
+                                     sf_base + slot0 * kSfColsPerChunk, idesc, accum);
             if (kps == 2)
-              issue_chunk<false>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
-                                 sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
+              issue_chunk<PAIR, false>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4),
+                                       b_lo0 + (slot0 + 1) * b_stride16, sf_base + (slot0 + 1) * kSfColsPerChunk,
+                                       idesc, accum);
           }
-          mma_commit(smem_u32(&sh.empty[s]));
+          if (PAIR) mma_commit_pair(smem_u32(&sh.empty[s]), 3);
+          else mma_commit(smem_u32(&sh.empty[s]));
         }
         if (!ok) break;
-        mma_commit(smem_u32(&sh.acc_full[ab]));
+        if (PAIR) mma_commit_pair(smem_u32(&sh.acc_full[ab]), 3);
+        else mma_commit(smem_u32(&sh.acc_full[ab]));
         if (++ab == acc_bufs) {
           ab = 0;
           aph ^= 1u;
         }
       }
       // every MMA this thread issued has completed before TMEM is released
-      mma_commit(smem_u32(sh.drain));
+      if (PAIR) mma_commit_pair(smem_u32(sh.drain), 1);
+      else mma_commit(smem_u32(sh.drain));
       mbar_wait(smem_u32(sh.drain), 0, 100000000ull);
     }
   } else if (warp >= kWarpSf0 && warp < kWarpSf0 + 4) {
     // ================================================================ scale staging
     // Per stage: the weight (A) scale blocks of the tile's two row blocks (one
     // 16-byte word per lane and block, already in the tensor-memory order) and
-    // the token-row (B) scales (one 32-bit word per row and chunk) are read from
-    // global memory -- issued before the slot is free: the ring gives them S
-    // stages of lead -- and stored with tcgen05.st into this warp's TMEM lane
-    // quarter (all four quarters hold the same words, the layout the block-
-    // scaled MMA reads).  The warp then arrives on the stage's full barrier.
+    // the token-row (B) scales (one 32-bit word per row and chunk, all N rows
+    // of the tile also with a pair) are read from global memory -- issued
+    // before the slot is free: the ring gives them S stages of lead -- and
+    // stored with tcgen05.st into this warp's TMEM lane quarter (all four
+    // quarters hold the same words, the layout the block-scaled MMA reads).
+    // The warp then arrives on the stage's full barrier.
     const int q = warp & 3;
     const int K32 = p.K / 32;
     const uint32_t S_ = static_cast<uint32_t>(S);
@@ -439,9 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t rs = 0, rph = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
-      const bool two = 2 * tl.m + 1 < p.RB;
+      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
+      const bool two = 2 * m + 1 < p.RB;
       // rows 32j + lane of this tile: their scale rows (null: a padding row)
       const uint32_t* rowp[8];
 #pragma unroll
@@ -468,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sft = tid - kWarpSf0 * 32;
         for (int i = sft; i < NK * lines; i += 128) {
           const int kc = i / lines, line = i - kc * lines;
-          const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * tl.m) * 32;
+          const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * m) * 32;
           prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
         }
       }
@@ -486,12 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 8; ++j) bw[u][j] = (u < kps && rowp[j]) ? __ldg(rowp[j] + ks + u) : 0x7F7F7F7Fu;
           a0[u] = a1[u] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
           if (u < kps) {
-            const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + ks + u) * p.RB + 2 * tl.m) * 32;
+            const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + ks + u) * p.RB + 2 * m) * 32;
             a0[u] = __ldg(blk + lane);
             if (two) a1[u] = __ldg(blk + 32 + lane);
           }
         }
-        if (!warp_wait_bar(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
+        if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
           ok = false;
           break;
         }
@@ -511,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.full[s]));
+        if (lane == 0) arrive_leader<PAIR>(sh, &sh.full[s]);
       }
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
@@ -521,22 +598,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(p.epi);
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    for (int t = unit0; t < total; t += unit_step) {
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       ab = ab_next;
       aph = aph_next;
       if (++ab_next == acc_bufs) {
         ab_next = 0;
         aph_next ^= 1u;
       }
-      if (!warp_wait_bar(sh, &sh.acc_full[ab], aph, p.wait_limit_ns, p.status)) break;
+      if (!warp_wait_bar<PAIR>(sh, &sh.acc_full[ab], aph, p.wait_limit_ns, p.status)) break;
       tc_fence_after();
       __syncwarp();
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t d0 = tbase + lane_base + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
       const uint32_t d1 = tbase + lane_base + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
       if (p.epi == 0) {
-        const int i0 = tl.m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
+        const int i0 = m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
         const int I = p.I, I32 = p.I / 32;
         uint8_t* const h_codes = p.h_codes;
         uint8_t* const h_scales = p.h_scales;
@@ -585,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
       } else {
-        const bool two = 2 * tl.m + 1 < p.RB;
+        const bool two = 2 * m + 1 < p.RB;
         float* const out = p.out;
         const int H = p.H;
         float* const ebf = reinterpret_cast<float*>(ebuf);
@@ -605,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           for (int sub = 0; sub < (two ? 2 : 1); ++sub) {
             const uint32_t d = sub == 0 ? d0 : d1;
-            const int o0 = tl.m * 256 + sub * 128 + 32 * q;  // this warp's 32 rows of H
+            const int o0 = m * 256 + sub * 128 + 32 * q;  // this warp's 32 rows of H
             for (int h0 = 0; h0 < 32 && c0 + h0 < tl.rows; h0 += 16) {
               uint32_t a[16];
               __syncwarp();
@@ -636,16 +714,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.acc_empty[ab]));
+      if (lane == 0) arrive_leader<PAIR>(sh, &sh.acc_empty[ab]);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) {
+    // neither CTA of the pair leaves (or frees tensor memory, which is
+    // allocated and freed by both at once) while the other can still arrive
+    // on its barriers, load into its shared memory or be written by its MMAs:
+    // each tells the other that all its roles are done (rank 0's MMAs have
+    // drained by then) and waits for the same word from the other
+    if (tid == 0) {
+      mbar_arrive_cluster(mapa_shared(smem_u32(sh.exit_bar), sh.rank ^ 1u));
+      const uint64_t t0 = globaltimer_ns();
+      const unsigned long long lim = 8ull * p.wait_limit_ns + 100000000ull;
+      while (!mbar_try_wait_cluster_sleep(smem_u32(sh.exit_bar), 0u, 20000u)) {
+        if (globaltimer_ns() - t0 > lim) {
+          set_status(p.status, MX_ERR_TIMEOUT);
+          break;
+        }
+      }
+      if (*sh.abort_flag) {
+        // an aborted pair may still have TMA loads in flight into this CTA's
+        // shared memory that no barrier here tracks: let them land
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+      }
+    }
+    __syncthreads();
+  }
   tc_fence_after();
   if (warp == kWarpMma) {
     __syncwarp();
-    tmem_dealloc(tbase, kTmemCols);
+    if (PAIR) tmem_dealloc_pair(tbase, kTmemCols);
+    else tmem_dealloc(tbase, kTmemCols);
   }
 }
 
@@ -679,9 +784,18 @@ static int sm_count_gemm() {
 // shared memory).
 static uint32_t weight_block_tx_bytes(int fmt) { return fmt == MX_E4M3 ? 16384u : 8192u; }
 
+bool pair_supported(const GemmArgs& a) {
+  // both CTAs of a pair take full two-block weight tiles, with token rows in
+  // slot order (2-D boxes)
+  const int rows = a.epi == 0 ? 2 * a.I : a.H;
+  return !a.gather4 && (rows / 128) % 4 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
+}
+
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
+  const bool pair = a.pair != 0;
+  if (pair && !pair_supported(a)) return cudaErrorInvalidConfiguration;
   GemmParams p{};
   p.epi = a.epi;
   p.afmt = a.fmt;
@@ -695,6 +809,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.NK = p.K / 128;
   p.RB = rows / 128;
   p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
+  if (pair) p.NM /= 2;   // pair tiles: two weight tiles each
   // down GEMM: split the weight tiles into groups so that one group's slice of
   // `out` (T rows x the group's 256-column blocks, fp32) stays within ~16 MB of
   // L2 while every expert's atomic combine lands on it
@@ -710,6 +825,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     p.MG = p.NM / groups;
   }
   p.bn = a.bn;
+  p.brows = pair ? a.bn / 2 : a.bn;
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
   const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt, a.epi == 0 ? 1 : 0);
@@ -742,7 +858,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     *acc_bufs = (4u * static_cast<uint32_t>(p.bn) + 2u * kSfColsPerChunk * kps <= kTmemCols) ? 2 : 1;
     *sf_col0 = 2u * static_cast<uint32_t>(*acc_bufs) * static_cast<uint32_t>(p.bn);
     if (*sf_col0 + 2u * kSfColsPerChunk * kps > kTmemCols) return 0;
-    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.bn) * 128u) * static_cast<uint32_t>(kps);
+    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.brows) * 128u) * static_cast<uint32_t>(kps);
     if (static_cast<uint32_t>(max_smem) <= fixed) return 0;
     int st = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
     if (st > kMaxStages) st = kMaxStages;
@@ -774,7 +890,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.off_a = off;
   off += static_cast<uint32_t>(stages * p.kps) * 32768u;
   p.off_b = off;
-  off += static_cast<uint32_t>(stages * p.kps) * p.bn * 128u;
+  off += static_cast<uint32_t>(stages * p.kps) * p.brows * 128u;
   p.off_meta = off;
   off += meta_bytes;
   p.off_bar = off;
@@ -808,11 +924,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   {
     // gather4: the activation matrix [T, H], four token rows at a time (box one
-    // row high); otherwise slot-ordered rows [n_rows, K], one bn-row box per stage
+    // row high); otherwise slot-ordered rows [n_rows, K], one box of `brows`
+    // rows per stage (bn, or half of it for each CTA of a pair)
     const cuuint64_t b_rows = static_cast<cuuint64_t>(p.gather4 ? a.T : a.n_rows);
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), b_rows};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-    cuuint32_t box[2] = {128, p.gather4 ? 1u : static_cast<cuuint32_t>(p.bn)};
+    cuuint32_t box[2] = {128, p.gather4 ? 1u : static_cast<cuuint32_t>(p.brows)};
     cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.b_codes), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -820,24 +937,26 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
 
-  // the shared-memory opt-in is per device and only ever raised: skip the
-  // driver call when a launch on this device already allowed this much
+  auto kernel = pair ? k_grouped_gemm<true> : k_grouped_gemm<false>;
+  // the shared-memory opt-in is per device and kernel and only ever raised:
+  // skip the driver call when a launch on this device already allowed this much
   {
-    static std::atomic<int> smem_allowed[kMaxDevices];
-    if (dev < 0 || dev >= kMaxDevices || smem_allowed[dev].load(std::memory_order_relaxed) < static_cast<int>(smem)) {
-      cudaError_t e = cudaFuncSetAttribute(k_grouped_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
+    static std::atomic<int> smem_allowed[2][kMaxDevices];
+    std::atomic<int>* allowed = (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[pair ? 1 : 0][dev] : nullptr;
+    if (!allowed || allowed->load(std::memory_order_relaxed) < static_cast<int>(smem)) {
+      cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < kMaxDevices) smem_allowed[dev].store(static_cast<int>(smem), std::memory_order_relaxed);
+      if (allowed) allowed->store(static_cast<int>(smem), std::memory_order_relaxed);
     }
   }
-  // upper bound on tiles: NM * sum_e ceil(count_e / bn) <= NM * (E + 1 + rows / bn)
+  // upper bound on work units: NM * sum_e ceil(count_e / bn) <= NM * (E + 1 + rows / bn)
   const long long bound =
       static_cast<long long>(p.NM) * (a.E + 1 + (a.n_rows + p.bn - 1) / p.bn);
-  int grid = sm_count_gemm();
-  if (bound < grid) grid = static_cast<int>(bound > 0 ? bound : 1);
-  if (!a.pdl) {
-    k_grouped_gemm<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
+  int units = sm_count_gemm() / (pair ? 2 : 1);
+  if (bound < units) units = static_cast<int>(bound > 0 ? bound : 1);
+  const int grid = units * (pair ? 2 : 1);
+  if (!a.pdl && !pair) {
+    kernel<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -845,12 +964,23 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (a.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (pair) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_grouped_gemm, p, tm_a, tm_b);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kernel, p, tm_a, tm_b);
 }
 
 }  // namespace mxk

@@ -93,13 +93,17 @@ struct GemmArgs {
   uint8_t* h_scales;        // GEMM1 out
   float* out;               // GEMM2 out
   int* status;
-  int bn;                   // N tile (32 or 128)
+  int bn;                   // token-tile width (16 .. 224; a pair's tile spans both CTAs)
   uint64_t wait_limit_ns;
   // programmatic dependent launch: 0 none; 1 the previous grid produced the
   // offsets and the B rows (wait before anything); 2 the previous grid produced
   // only the B rows and their scales (weights stream before the wait)
   int pdl;
+  // run as clusters of two CTAs with the pair MMA (M = 256 over two SMs; each
+  // SM loads half of the token rows); needs pair_supported()
+  int pair;
 };
+bool pair_supported(const GemmArgs& a);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
 }  // namespace mxk

@@ -210,6 +210,10 @@ LAYER_CASES = {
     "one_token": W.custom("one_token", T=1, H=256, I=128, E=4, k=2, fmt="e4m3"),
     "one_expert": W.custom("one_expert", T=5, H=128, I=128, E=1, k=1, fmt="e2m1"),
     "k_equals_e": W.custom("k_equals_e", T=9, H=256, I=256, E=4, k=4, fmt="e4m3"),
+    # wide schedule as CTA pairs in both GEMMs (every pair tile has four weight
+    # row blocks), skewed experts: many token tiles, one partial tile, a few rows
+    "pair_e4m3": W.custom("pair_e4m3", T=1500, H=512, I=512, E=16, k=4, fmt="e4m3", zipf_bias=True),
+    "pair_e2m1": W.custom("pair_e2m1", T=900, H=1024, I=256, E=6, k=2, fmt="e2m1", zipf_bias=True),
     # the routing limits: 1024 routed experts (+1 shared), top-32
     "max_routing": W.custom("max_routing", T=40, H=128, I=128, E=1024, k=32, fmt="e2m1"),
 }
@@ -364,3 +368,25 @@ def test_layer_parity_down_tile_groups(name, groups, monkeypatch):
     assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
     rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
     assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+
+
+@pytest.mark.parametrize("name,bn", [("pair_e4m3", None), ("pair_e2m1", None), ("wide_e4m3", "128"),
+                                     ("pair_e4m3", "96"), ("pair_e4m3", "224")])
+def test_pair_schedule_matches_single_cta(name, bn, monkeypatch):
+    """The wide schedule run as CTA pairs (M = 256 MMAs over two SMs) and as
+    single CTAs gives the same layer, and both match the oracle."""
+    if bn:
+        monkeypatch.setenv("MXMOE_BN", bn)
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle_forward(L)
+    outs = {}
+    for pair in ("1", "0"):
+        monkeypatch.setenv("MXMOE_PAIR", pair)
+        out = L.layer.forward(L.x, L.logits)
+        assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+        rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+        assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (pair, rel, mabs)
+        outs[pair] = out
+    diff = (outs["1"] - outs["0"]).abs().max().item() / outs["0"].abs().max().item()
+    assert diff < 1e-5, diff
