@@ -51,12 +51,15 @@ int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
   return MX_OK;
 }
 
-// The wide schedule runs the grouped GEMMs as CTA pairs (M = 256 MMAs over two
-// SMs, each loading half of a tile's token rows) when every pair tile has its
-// full four weight row blocks; MXMOE_PAIR=0 turns that off (A/B runs).
+// The wide schedule can run the grouped GEMMs as CTA pairs (M = 256 MMAs over
+// two SMs, each loading half of a tile's token rows) when every pair tile has
+// its full four weight row blocks.  Measured on the 8192-token prefill layer,
+// pairs were slower than single CTAs (gate/up 1.24 vs 1.10 ms: the per-SM
+// operand rate did not rise and the pair waits for both epilogues between
+// tiles), so they run only when MXMOE_PAIR=1 asks for them (A/B runs, tests).
 void choose_pair(GemmArgs& a) {
   const char* env = std::getenv("MXMOE_PAIR");
-  a.pair = (!a.gather4 && !(env && env[0] == '0') && pair_supported(a)) ? 1 : 0;
+  a.pair = (!a.gather4 && env && env[0] == '1' && pair_supported(a)) ? 1 : 0;
 }
 
 // The narrow schedule gathers each tile's few token rows with TMA gather4; the

@@ -18,18 +18,20 @@
 // stage is full once its TMA bytes have landed and the scale-staging warps
 // have put its scale factors into tensor memory.
 //
-// Warp roles (512 threads):
+// Warp roles (448 threads):
 //   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
 //               unpacked to the 16-byte-aligned form by the TMA) and token
 //               rows (tensor map)
 //   warp 1      TMEM allocation; one thread issues
-//               tcgen05.mma.kind::mxf8f6f4.block_scale
-//   warps 4-7   scale staging: the weight and token-row scale factors of
+//               tcgen05.mma.kind::mxf8f6f4.block_scale (with a CTA pair:
+//               rank 0; rank 1's thread relays its stage completions)
+//   warps 2-5   scale staging: the weight and token-row scale factors of
 //               every stage, from global memory into every TMEM lane quarter
 //               with tcgen05.st
-//   warps 8-15  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
+//   warps 6-13  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
 //               MXFP8 re-quantisation or weighted combine; warps w and w + 4
-//               share a TMEM lane quarter and take alternate column chunks
+//               share a TMEM lane quarter (w mod 4) and take alternate column
+//               chunks
 // Every wait is bounded (wall clock); a wait that runs out sets
 // MX_ERR_TIMEOUT in the status word and every role unwinds.
 #include <cuda.h>
@@ -45,11 +47,11 @@
 
 namespace mxk {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 448;
 constexpr int kWarpTma = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpSf0 = 4;
-constexpr int kWarpEpi0 = 8;
+constexpr int kWarpMma = 1;     // with a CTA pair, rank 1's warp relays stage completions
+constexpr int kWarpSf0 = 2;     // warps 2..5: TMEM lane quarters 2, 3, 0, 1
+constexpr int kWarpEpi0 = 6;    // warps 6..13: two per lane quarter
 constexpr int kEpiWarps = 8;
 // per epilogue warp, a transpose tile: 16 columns of E4M3 codes (gate/up) or
 // 8 columns of fp32 (down)
@@ -85,6 +87,7 @@ struct GemmParams {
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
   int pdl;          // see GemmArgs::pdl
   int kps;          // 128-wide K chunks per pipeline stage (1 or 2)
+  uint32_t hint_ns; // pair: suspend-time hint of whole-warp barrier waits (0: spin)
 };
 
 struct Tile {
@@ -102,8 +105,11 @@ struct Shared {
   uint64_t* acc_empty;
   uint64_t* drain;
   uint64_t* exit_bar;  // CTA pair: the peer has finished every role
+  uint64_t* peer_full; // CTA pair, rank 0: rank 1's copy of the stage is full
   uint32_t* tmem_slot;
+  unsigned* sf_cnt;    // CTA pair: scale warps done with each pipeline slot
   uint32_t rank;       // rank in the CTA pair (0 without one)
+  uint32_t hint_ns;    // suspend-time hint of whole-warp waits (0: spin on test_wait)
 };
 
 // Tile t -> (group, expert, token tile, weight tile).  Tiles are ordered group-
@@ -147,7 +153,10 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint64_t* bar, uint32
                                          unsigned long long limit_ns, int* status) {
   const uint32_t b = smem_u32(bar);
   auto poll = [&](bool sleep) {
-    if (PAIR) return sleep ? mbar_try_wait_cluster_sleep(b, parity, 20000u) : mbar_try_wait_cluster(b, parity);
+    if (PAIR) {
+      if (!sleep) return mbar_try_wait_cluster(b, parity);
+      return sh.hint_ns ? mbar_try_wait_cluster_sleep(b, parity, sh.hint_ns) : mbar_test_wait_cluster(b, parity);
+    }
     return sleep ? mbar_try_wait_sleep(b, parity, 20000u) : mbar_try_wait(b, parity);
   };
   if (poll(false)) return true;
@@ -234,7 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.exit_bar = bars + 2 * S + 5;
   sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
   sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 7);
+  sh.peer_full = bars + 2 * S + 8;                                 // S barriers
+  sh.sf_cnt = reinterpret_cast<unsigned*>(bars + 3 * S + 8);       // S counters
   sh.rank = PAIR ? cluster_ctarank() : 0u;
+  sh.hint_ns = p.hint_ns;
   const bool leader = sh.rank == 0;
   // work units: one per CTA, or one per CTA pair
   const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
@@ -247,11 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // a stage is full when its TMA bytes have landed (producer: 1 arrival
-      // with the byte count; a pair's rank 0 counts both CTAs' bytes) and the
-      // scale-staging warps have put its scale factors into tensor memory (4
-      // arrivals per CTA)
-      mbar_init(smem_u32(&sh.full[s]), PAIR ? 9 : 5);
+      // with the byte count) and the scale-staging warps have put its scale
+      // factors into tensor memory (4 arrivals; with a pair, 1).  In a pair
+      // each CTA's full barrier tracks its own copy of the stage, and rank 1
+      // relays its completion to rank 0's peer_full barrier.
+      mbar_init(smem_u32(&sh.full[s]), PAIR ? 2 : 5);
       mbar_init(smem_u32(&sh.empty[s]), 1);
+      mbar_init(smem_u32(&sh.peer_full[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.acc_full[a]), 1);
@@ -259,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(sh.drain), 1);
     mbar_init(smem_u32(sh.exit_bar), 1);
+    for (int s = 0; s < S; ++s) sh.sf_cnt[s] = 0u;
     *sh.abort_flag = 0;
     fence_mbar_init();
   }
@@ -364,19 +379,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t full = PAIR ? mapa_shared(smem_u32(&sh.full[s]), 0u) : smem_u32(&sh.full[s]);
+        const uint32_t full = smem_u32(&sh.full[s]);
         const uint32_t su = s * static_cast<uint32_t>(kps);  // first chunk slot
         if (lane == 0) {
-          if (!PAIR) mbar_arrive_expect_tx(full, bytes);
-          else if (leader) mbar_arrive_expect_tx_cluster(full, 2u * bytes);   // both CTAs' loads
+          mbar_arrive_expect_tx(full, bytes);
           for (int u = 0; u < kps; ++u) {
             const int kc = ks + u;
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
             // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
             // the TMA fills zeros and still counts the whole box)
             const int blk0 = (tl.e * NK + kc) * p.RB + 2 * m;
-            if (PAIR) tma_load_3d_pair(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
-            else tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
+            tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
           }
         }
         if (!b_ready) {
@@ -386,10 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = 0; u < kps; ++u) {
           const int kc = ks + u;
           const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.brows * 128u);
-          if (lane == 0 && !gather) {
-            if (PAIR) tma_load_2d_pair(b_s, &tm_b, kc * 128, b_row0, full);
-            else tma_load_2d(b_s, &tm_b, kc * 128, b_row0, full);
-          }
+          if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, b_row0, full);
           __syncwarp();
           if (gather && lane < n4)
             tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
@@ -402,14 +412,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // drain: every fill this warp armed has landed before the CTA exits (a
-    // pair's rank 0 counts both CTAs' loads on its full barriers; rank 1 is
-    // held at the exit handshake until rank 0 has drained)
-    if (lane == 0 && (!PAIR || leader)) {
+    // drain: every fill this warp armed has landed before the CTA exits
+    if (lane == 0) {
       const uint32_t n_fills = it;
       for (int s = 0; s < S && static_cast<uint32_t>(s) < n_fills; ++s) {
         const uint32_t last = n_fills - 1 - ((n_fills - 1 - s) % S);
         mbar_wait(smem_u32(&sh.full[s]), (last / S) & 1u, 100000000ull);
+      }
+    }
+  } else if (PAIR && warp == kWarpMma && !leader) {
+    // ================================================================ pair relay
+    // Rank 1 (whose MMA warp issues nothing): once its copy of a stage is full
+    // (its TMA bytes landed, its scale factors stored), tell rank 0, whose
+    // MMAs read both copies.
+    if (lane == 0) {
+      const uint32_t S_ = static_cast<uint32_t>(S);
+      const int NKs = NK / p.kps;
+      uint32_t rs = 0, rph = 0;
+      bool ok = true;
+      for (int t = unit0; t < total && ok; t += unit_step) {
+        for (int ks = 0; ks < NKs; ++ks) {
+          const uint32_t s = rs, ph = rph;
+          if (++rs == S_) {
+            rs = 0;
+            rph ^= 1u;
+          }
+          if (!wait_bar<PAIR, false>(sh, &sh.full[s], ph, p.wait_limit_ns, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_cluster(mapa_shared(smem_u32(&sh.peer_full[s]), 0u));
+        }
       }
     }
   } else if (warp == kWarpMma) {
@@ -455,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             rs = 0;
             rph ^= 1u;
           }
-          if (!wait_bar<PAIR, false>(sh, &sh.full[s], ph, lim, status)) {
+          if (!wait_bar<PAIR, false>(sh, &sh.full[s], ph, lim, status) ||
+              (PAIR && !wait_bar<PAIR, false>(sh, &sh.peer_full[s], ph, lim, status))) {
             ok = false;
             break;
           }
@@ -499,11 +533,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Per stage: the weight (A) scale blocks of the tile's two row blocks (one
     // 16-byte word per lane and block, already in the tensor-memory order) and
     // the token-row (B) scales (one 32-bit word per row and chunk, all N rows
-    // of the tile also with a pair) are read from global memory -- issued
-    // before the slot is free: the ring gives them S stages of lead -- and
-    // stored with tcgen05.st into this warp's TMEM lane quarter (all four
-    // quarters hold the same words, the layout the block-scaled MMA reads).
-    // The warp then arrives on the stage's full barrier.
+    // of the tile also with a pair) are read from global memory two K chunks
+    // ahead of the chunk being stored (three register buffers: a chunk's loads
+    // are in flight while earlier chunks wait for their slot and are stored),
+    // then stored with tcgen05.st into this warp's TMEM lane quarter
+    // (all four quarters hold the same words, the layout the block-scaled MMA
+    // reads).  Then the stage's full barrier gets its arrival: one per warp,
+    // or, with a pair, one for all four warps from the last of them to finish.
+    struct ScaleBuf {  // one K chunk
+      uint32_t bw[8];
+      uint4 a0, a1;
+    };
     const int q = warp & 3;
     const int K32 = p.K / 32;
     const uint32_t S_ = static_cast<uint32_t>(S);
@@ -512,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* const status = p.status;
     const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0;
     const uint4* const wsc = reinterpret_cast<const uint4*>(p.w_scales);
+    const uint32_t* const bsc = reinterpret_cast<const uint32_t*>(p.b_scales);
     uint32_t rs = 0, rph = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -519,12 +560,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
       const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       const bool two = 2 * m + 1 < p.RB;
-      // rows 32j + lane of this tile: their scale rows (null: a padding row)
-      const uint32_t* rowp[8];
+      // rows 32j + lane of this tile: the word offset of their scale rows
+      // (-1: a padding row)
+      int roww[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const int r = 32 * j + lane;
-        rowp[j] = nullptr;
+        roww[j] = -1;
         if (r < tl.rows) {
           int src_row = tl.p0 + r;
           if (p.epi == 0) {
@@ -534,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               src_row = 0;
             }
           }
-          rowp[j] = reinterpret_cast<const uint32_t*>(p.b_scales + static_cast<size_t>(src_row) * K32);
+          roww[j] = src_row * (K32 / 4);
         }
       }
       // warm L2 with the tile's weight-scale blocks (128-byte lines, 4 per
@@ -549,46 +591,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
         }
       }
-      for (int ks = 0; ks < NK; ks += kps) {
-        const uint32_t s = rs, ph = rph;
-        if (++rs == S_) {
-          rs = 0;
-          rph ^= 1u;
-        }
-        uint32_t bw[2][8];
-        uint4 a0[2], a1[2];
+      auto load = [&](ScaleBuf& b, int kc) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) bw[u][j] = (u < kps && rowp[j]) ? __ldg(rowp[j] + ks + u) : 0x7F7F7F7Fu;
-          a0[u] = a1[u] = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
-          if (u < kps) {
-            const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + ks + u) * p.RB + 2 * m) * 32;
-            a0[u] = __ldg(blk + lane);
-            if (two) a1[u] = __ldg(blk + 32 + lane);
+        for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bsc + roww[j] + kc) : 0x7F7F7F7Fu;
+        const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * m) * 32;
+        b.a0 = __ldg(blk + lane);
+        b.a1 = two ? __ldg(blk + 32 + lane) : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      };
+      // store chunk kc from `cur` (its loads issued two chunks earlier) after
+      // issuing the loads of chunk kc + 2 into `nxt`; the stage's slot is
+      // awaited at its first chunk and its arrival made after its last
+      uint32_t s = 0;
+      auto step = [&](ScaleBuf& cur, ScaleBuf& nxt, int kc) {
+        if (kc + 2 < NK) load(nxt, kc + 2);
+        const int u = kc % kps;
+        if (u == 0) {
+          s = rs;
+          const uint32_t ph = rph;
+          if (++rs == S_) {
+            rs = 0;
+            rph ^= 1u;
           }
+          if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) return false;
         }
-        if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
+        // chunk slot: A scales of row block 2m at +0, of 2m + 1 at +8, B at
+        // +16 (column j of a block holds rows 32j + lane; B: j < 8, N <= 256)
+        const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + static_cast<uint32_t>(u)) * kSfColsPerChunk;
+        __syncwarp();
+        tmem_st_32x32b_x4(col + 0u, cur.a0.x, cur.a0.y, cur.a0.z, cur.a0.w);
+        tmem_st_32x32b_x4(col + 8u, cur.a1.x, cur.a1.y, cur.a1.z, cur.a1.w);
+        if (bn > 128) tmem_st_32x32b_x8(col + 16u, cur.bw);
+        else tmem_st_32x32b_x4(col + 16u, cur.bw[0], cur.bw[1], cur.bw[2], cur.bw[3]);
+        if (u != kps - 1) return true;
+        tmem_st_wait();
+        tc_fence_before();
+        if (PAIR) {
+          // the last of the four scale warps to finish this stage (a shared
+          // counter per slot, reset by that warp; nothing blocks) arrives for all
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence_block();
+            if (atomicAdd(&sh.sf_cnt[s], 1u) == 3u) {
+              __threadfence_block();
+              sh.sf_cnt[s] = 0u;
+              mbar_arrive(smem_u32(&sh.full[s]));
+            }
+          }
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&sh.full[s]));
+        }
+        return true;
+      };
+      ScaleBuf b0, b1, b2;
+      load(b0, 0);
+      if (NK > 1) load(b1, 1);
+      for (int kc = 0; kc < NK; kc += 3) {
+        if (!step(b0, b2, kc)) {
           ok = false;
           break;
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          if (u < kps) {
-            // chunk slot: A scales of row block 2m at +0, of 2m + 1 at +8, B at
-            // +16 (column j of a block holds rows 32j + lane; B: j < 8, N <= 256)
-            const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + u) * kSfColsPerChunk;
-            __syncwarp();
-            tmem_st_32x32b_x4(col + 0u, a0[u].x, a0[u].y, a0[u].z, a0[u].w);
-            tmem_st_32x32b_x4(col + 8u, a1[u].x, a1[u].y, a1[u].z, a1[u].w);
-            if (bn > 128) tmem_st_32x32b_x8(col + 16u, bw[u]);
-            else tmem_st_32x32b_x4(col + 16u, bw[u][0], bw[u][1], bw[u][2], bw[u][3]);
-          }
+        if (kc + 1 >= NK) break;
+        if (!step(b1, b0, kc + 1)) {
+          ok = false;
+          break;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) arrive_leader<PAIR>(sh, &sh.full[s]);
+        if (kc + 2 >= NK) break;
+        if (!step(b2, b1, kc + 2)) {
+          ok = false;
+          break;
+        }
       }
     }
   } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
@@ -618,35 +690,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int I = p.I, I32 = p.I / 32;
         uint8_t* const h_codes = p.h_codes;
         uint8_t* const h_scales = p.h_scales;
-        // 16 columns at a time, each step over all 16 so that the per-column
-        // chains (SwiGLU, warp amax, exponent, encode) overlap
-        for (int c0 = 16 * half; c0 < tl.rows; c0 += 32) {
-          uint32_t g[16], u[16];
-          __syncwarp();
-          tmem_ld_32x32b_x16(d0 + c0, g);
-          tmem_ld_32x32b_x16(d1 + c0, u);
-          tmem_ld_wait();
-          float h[16];
-          uint32_t amax[16];
+        // 8 columns at a time, each step over all 8 so that the per-column
+        // chains (SwiGLU, warp amax, exponent, encode) overlap; the tensor-
+        // memory loads of the warp's next 8 columns are in flight while the
+        // current ones are processed (two register sets, computed in place)
+        auto process = [&](uint32_t (&g)[8], uint32_t (&u)[8], int c0) {
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
+          for (int cc = 0; cc < 8; ++cc) {
             // silu(g) * u with the fast reciprocal: h is re-quantised to 3
             // mantissa bits right after, far coarser than its 2-ulp error
             const float gv = __uint_as_float(g[cc]);
-            h[cc] = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
-            amax[cc] = __float_as_uint(h[cc]) & 0x7FFFFFFFu;
+            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
+            g[cc] = __float_as_uint(hv);
+            u[cc] = __float_as_uint(hv) & 0x7FFFFFFFu;
           }
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) amax[cc] = __reduce_max_sync(0xffffffffu, amax[cc]);
-          // codes go through a per-warp shared-memory tile [16 columns][32 rows
+          for (int cc = 0; cc < 8; ++cc) u[cc] = __reduce_max_sync(0xffffffffu, u[cc]);
+          // codes go through a per-warp shared-memory tile [8 columns][32 rows
           // of I] so that each lane writes one 16-byte run of an h row (byte
           // stores from every lane, one per column, throttle the store path)
-          int my_s = 0;  // lane j < 16: the scale of column j
+          int my_s = 0;  // lane j < 8: the scale of column j
 #pragma unroll
-          for (int cc = 0; cc < 16; cc += 2) {
-            const int s0 = mx_block_exponent(amax[cc], 8);
-            const int s1 = mx_block_exponent(amax[cc + 1], 8);
-            const uint32_t codes = enc_e4m3x2(h[cc] * pow2_neg(s0), h[cc + 1] * pow2_neg(s1));
+          for (int cc = 0; cc < 8; cc += 2) {
+            const int s0 = mx_block_exponent(u[cc], 8);
+            const int s1 = mx_block_exponent(u[cc + 1], 8);
+            const uint32_t codes =
+                enc_e4m3x2(__uint_as_float(g[cc]) * pow2_neg(s0), __uint_as_float(g[cc + 1]) * pow2_neg(s1));
             ebuf[cc * 32 + lane] = static_cast<uint8_t>(codes);
             ebuf[(cc + 1) * 32 + lane] = static_cast<uint8_t>(codes >> 8);
             if (lane == cc) my_s = s0;
@@ -655,12 +724,41 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           const int nvalid = tl.rows - c0;
           const int col = lane >> 1;
-          const uint4 v = *reinterpret_cast<const uint4*>(ebuf + col * 32 + (lane & 1) * 16);
-          if (col < nvalid)
-            *reinterpret_cast<uint4*>(h_codes + static_cast<size_t>(tl.p0 + c0 + col) * I + i0 + (lane & 1) * 16) = v;
-          if (lane < 16 && lane < nvalid)
+          if (lane < 16) {
+            const uint4 v = *reinterpret_cast<const uint4*>(ebuf + col * 32 + (lane & 1) * 16);
+            if (col < nvalid)
+              *reinterpret_cast<uint4*>(h_codes + static_cast<size_t>(tl.p0 + c0 + col) * I + i0 + (lane & 1) * 16) = v;
+          }
+          if (lane < 8 && lane < nvalid)
             h_scales[static_cast<size_t>(tl.p0 + c0 + lane) * I32 + i0 / 32] = static_cast<uint8_t>(my_s + 127);
           __syncwarp();
+        };
+        uint32_t ga[8], ua[8], gb[8], ub[8];
+        int c0 = 8 * half;
+        if (c0 < tl.rows) {
+          __syncwarp();
+          tmem_ld_32x32b_x8(d0 + c0, ga);
+          tmem_ld_32x32b_x8(d1 + c0, ua);
+          tmem_ld_wait();
+        }
+        while (c0 < tl.rows) {
+          const int c1 = c0 + 16;
+          if (c1 < tl.rows) {
+            tmem_ld_32x32b_x8(d0 + c1, gb);
+            tmem_ld_32x32b_x8(d1 + c1, ub);
+          }
+          process(ga, ua, c0);
+          if (c1 >= tl.rows) break;
+          tmem_ld_wait();
+          const int c2 = c1 + 16;
+          if (c2 < tl.rows) {
+            tmem_ld_32x32b_x8(d0 + c2, ga);
+            tmem_ld_32x32b_x8(d1 + c2, ua);
+          }
+          process(gb, ub, c1);
+          if (c2 >= tl.rows) break;
+          tmem_ld_wait();
+          c0 = c2;
         }
       } else {
         const bool two = 2 * m + 1 < p.RB;
@@ -682,13 +780,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           for (int sub = 0; sub < (two ? 2 : 1); ++sub) {
+            // both 16-column halves of this row block's 32 columns in flight at
+            // once, then one wait
             const uint32_t d = sub == 0 ? d0 : d1;
+            uint32_t a[2][16];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+              if (c0 + 16 * hh < tl.rows) tmem_ld_32x32b_x16(d + c0 + 16 * hh, a[hh]);
+            tmem_ld_wait();
             const int o0 = m * 256 + sub * 128 + 32 * q;  // this warp's 32 rows of H
-            for (int h0 = 0; h0 < 32 && c0 + h0 < tl.rows; h0 += 16) {
-              uint32_t a[16];
-              __syncwarp();
-              tmem_ld_32x32b_x16(d + c0 + h0, a);
-              tmem_ld_wait();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int h0 = 16 * hh;
+              if (c0 + h0 >= tl.rows) break;
               // weighted values through the per-warp transpose tile [8 columns]
               // [32 rows of H], then four consecutive H values per lane and
               // column: one 16-byte vector reduction instead of four scalar ones
@@ -696,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int c8 = 0; c8 < 16; c8 += 8) {
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc)
-                  ebf[cc * 32 + lane] = __shfl_sync(0xffffffffu, wt, h0 + c8 + cc) * __uint_as_float(a[c8 + cc]);
+                  ebf[cc * 32 + lane] = __shfl_sync(0xffffffffu, wt, h0 + c8 + cc) * __uint_as_float(a[hh][c8 + cc]);
                 __syncwarp();
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
@@ -734,13 +838,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (globaltimer_ns() - t0 > lim) {
           set_status(p.status, MX_ERR_TIMEOUT);
           break;
-        }
-      }
-      if (*sh.abort_flag) {
-        // an aborted pair may still have TMA loads in flight into this CTA's
-        // shared memory that no barrier here tracks: let them land
-        const uint64_t t0 = globaltimer_ns();
-        while (globaltimer_ns() - t0 < 200000ull) {
         }
       }
     }
@@ -841,6 +938,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.wait_limit_ns = a.wait_limit_ns;
   p.gather4 = a.gather4;
   p.pdl = a.pdl;
+  p.hint_ns = 20000u;
+  if (const char* env = std::getenv("MXMOE_PAIR_HINT_NS")) p.hint_ns = static_cast<uint32_t>(std::atoi(env));
 
   // shared memory and tensor memory plan for `kps` 128-wide K chunks per
   // pipeline stage: returns the stage count (0 if fewer than two fit)

@@ -373,8 +373,9 @@ def test_layer_parity_down_tile_groups(name, groups, monkeypatch):
 @pytest.mark.parametrize("name,bn", [("pair_e4m3", None), ("pair_e2m1", None), ("wide_e4m3", "128"),
                                      ("pair_e4m3", "96"), ("pair_e4m3", "224")])
 def test_pair_schedule_matches_single_cta(name, bn, monkeypatch):
-    """The wide schedule run as CTA pairs (M = 256 MMAs over two SMs) and as
-    single CTAs gives the same layer, and both match the oracle."""
+    """The wide schedule run as CTA pairs (M = 256 MMAs over two SMs, on
+    request) and as single CTAs gives the same layer, and both match the
+    oracle."""
     if bn:
         monkeypatch.setenv("MXMOE_BN", bn)
     wl = LAYER_CASES[name]
