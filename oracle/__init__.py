@@ -24,6 +24,8 @@ _lib = None
 
 E4M3 = 0
 E2M1 = 1
+ACT_SWIGLU = 0
+ACT_SWIGLU_OAI = 1
 
 
 def compile_library(src: str, out: str) -> str:
@@ -58,6 +60,10 @@ def _bind(L):
     L.orc_permute.argtypes = [P, i32, i32, i32, P, P, P]
     L.orc_expert_layer.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
                                    P, P, P, P]
+    L.orc_expert_layer_ex.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
+                                      P, P, P, P, i32, ctypes.c_double, ctypes.c_double, i32, i32]
+    L.orc_swiglu_oai.restype = ctypes.c_double
+    L.orc_swiglu_oai.argtypes = [ctypes.c_double] * 4
     L.orc_set_threads.argtypes = [i32]
     L.orc_set_threads.restype = None
     return L
@@ -122,9 +128,15 @@ def quantize_rows(v, fmt: int):
     return codes, scales
 
 
-def quantize_bf16(x_bits: np.ndarray):
-    """bf16 activations (uint16 bit patterns) [T, H] -> MXFP8 codes [T, H], scales [T, H/32]."""
+def quantize_bf16(x_bits: np.ndarray, fmt: int = E4M3):
+    """bf16 activations (uint16 bit patterns) [T, H] -> MX codes and scales
+    [T, H/32]: MXFP8 codes [T, H], or (fmt = E2M1) MXFP4 codes [T, H/2] packed
+    two per byte, element 2i in the low nibble (the bf16 values widened to
+    fp64 exactly and quantised by quantize_rows)."""
     x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    if fmt == E2M1:
+        widened = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        return quantize_rows(widened, E2M1)
     T, H = x.shape
     codes = np.zeros((T, H), dtype=np.uint8)
     scales = np.zeros((T, H // 32), dtype=np.uint8)
@@ -207,10 +219,14 @@ def permute(ids: np.ndarray, E: int):
 # ------------------------------------------------------------------ expert layer
 def expert_layer(act_codes, act_scales, ids, topk_w, w1c: Sequence, w1s: Sequence, w2c: Sequence,
                  w2s: Sequence, fmt: int, I: int, tokens: Optional[Sequence[int]] = None,
-                 want_h: bool = False, want_noq: bool = False):
-    """Grouped gate/up GEMM + SwiGLU + MXFP8 requant of h + down GEMM + weighted
-    combine, on already quantised activations.  Weight lists hold E+1 entries
-    (shared expert last); None is allowed for experts no requested token uses.
+                 want_h: bool = False, want_noq: bool = False, act: int = ACT_SWIGLU, alpha: float = 1.0,
+                 limit: float = float("inf"), act_fmt: int = E4M3):
+    """Grouped gate/up GEMM + SwiGLU (or SwiGLU-OAI with ``alpha`` and
+    ``limit``) + MX requant of h + down GEMM + weighted combine, on already
+    quantised activations.  ``act_fmt`` is the activations' MX format; h is
+    re-quantised to the same format (MXFP8, or MXFP4 for FP4 activations).
+    Weight lists hold E+1 entries (shared expert last); None is allowed for
+    experts no requested token uses.
 
     Returns dict with ``out`` fp64 [n_tokens, H] and optionally ``h_codes`` /
     ``h_scales`` (by slot id) and ``out_noq`` (h not re-quantised)."""
@@ -218,7 +234,8 @@ def expert_layer(act_codes, act_scales, ids, topk_w, w1c: Sequence, w1s: Sequenc
     act_scales = np.ascontiguousarray(act_scales, dtype=np.uint8)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     topk_w = np.ascontiguousarray(topk_w, dtype=np.float64)
-    T, H = act_codes.shape
+    T = act_codes.shape[0]
+    H = act_scales.shape[1] * 32
     k = ids.shape[1]
     E = len(w1c) - 1
     keep = []
@@ -239,12 +256,14 @@ def expert_layer(act_codes, act_scales, ids, topk_w, w1c: Sequence, w1s: Sequenc
     n = T if tok is None else tok.size
     out = np.zeros((n, H), dtype=np.float64)
     out_noq = np.zeros((n, H), dtype=np.float64) if want_noq else None
-    hc = np.zeros((T * (k + 1), I), dtype=np.uint8) if want_h else None
+    h_row = I if act_fmt == E4M3 else I // 2
+    hc = np.zeros((T * (k + 1), h_row), dtype=np.uint8) if want_h else None
     hs = np.zeros((T * (k + 1), I // 32), dtype=np.uint8) if want_h else None
-    st = lib().orc_expert_layer(_ptr(act_codes), _ptr(act_scales), T, H, I, E, k, _ptr(ids), _ptr(topk_w),
-                                ctypes.cast(A1c, ctypes.c_void_p), ctypes.cast(A1s, ctypes.c_void_p),
-                                ctypes.cast(A2c, ctypes.c_void_p), ctypes.cast(A2s, ctypes.c_void_p), fmt,
-                                _ptr(tok), n, _ptr(out), _ptr(out_noq), _ptr(hc), _ptr(hs))
+    st = lib().orc_expert_layer_ex(_ptr(act_codes), _ptr(act_scales), T, H, I, E, k, _ptr(ids), _ptr(topk_w),
+                                   ctypes.cast(A1c, ctypes.c_void_p), ctypes.cast(A1s, ctypes.c_void_p),
+                                   ctypes.cast(A2c, ctypes.c_void_p), ctypes.cast(A2s, ctypes.c_void_p), fmt,
+                                   _ptr(tok), n, _ptr(out), _ptr(out_noq), _ptr(hc), _ptr(hs), int(act),
+                                   float(alpha), float(limit), int(act_fmt), int(act_fmt))
     _check(st, "expert_layer")
     res = {"out": out}
     if want_h:
@@ -255,15 +274,25 @@ def expert_layer(act_codes, act_scales, ids, topk_w, w1c: Sequence, w1s: Sequenc
 
 
 def moe_forward(x_bits, logits, k: int, w1c, w1s, w2c, w2s, fmt: int, I: int, tokens=None, want_h=False,
-                want_noq=False):
+                want_noq=False, act: int = ACT_SWIGLU, alpha: float = 1.0, limit: float = float("inf"),
+                act_fmt: int = E4M3):
     """The whole layer: activation quantisation, routing, permutation (implicit
     in the expert visiting order) and the expert layer."""
-    act_codes, act_scales = quantize_bf16(x_bits)
+    act_codes, act_scales = quantize_bf16(x_bits, act_fmt)
     ids, w = route_topk(logits, k)
     res = expert_layer(act_codes, act_scales, ids, w, w1c, w1s, w2c, w2s, fmt, I, tokens=tokens, want_h=want_h,
-                       want_noq=want_noq)
+                       want_noq=want_noq, act=act, alpha=alpha, limit=limit, act_fmt=act_fmt)
     res.update(act_codes=act_codes, act_scales=act_scales, ids=ids, topk_w=w)
     return res
+
+
+def swiglu_oai(g, u, alpha: float, limit: float) -> np.ndarray:
+    """Elementwise SwiGLU-OAI of the oracle's C code (gate clamped above at
+    ``limit``, up to [-limit, limit], g * sigmoid(alpha * g) * (u + 1))."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.broadcast_to(np.asarray(u, dtype=np.float64), g.shape)
+    f = lib().orc_swiglu_oai
+    return np.array([f(float(a), float(b), float(alpha), float(limit)) for a, b in zip(g.ravel(), u.ravel())]).reshape(g.shape)
 
 
 def set_threads(n: int) -> None:

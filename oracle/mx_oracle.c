@@ -19,8 +19,10 @@
  *     expert with weight 1 (same page, Figure 4).
  *   - Token -> expert permutation: experts ascending (shared last), tokens
  *     ascending inside an expert.
- *   - Expert MLP: g = x.Wg, u = x.Wu, h = silu(g) * u, h re-quantised to MXFP8
- *     per 32 along I, y = h.Wd, out[t] += w * y  (the down projection with the
+ *   - Expert MLP: g = x.Wg, u = x.Wu, h = silu(g) * u (or the SwiGLU-OAI form
+ *     with a clamp limit and a sigmoid slope, same page, correctness passage),
+ *     h re-quantised per 32 along I to MXFP8 (MXFP4 when the activations are
+ *     MXFP4: the page's MXFP4 results), y = h.Wd, out[t] += w * y  (the down projection with the
  *     weighted combine, "Kimi K3 performance in vLLM: 2.8x throughput",
  *     section on fusing the MXFP4 top-k finalize into the epilogue).
  *
@@ -281,6 +283,23 @@ int orc_permute(const int32_t* ids, int T, int E, int k, int32_t* counts, int32_
 
 static double silu(double z) { return z / (1.0 + exp(-z)); }
 
+#define ORC_ACT_SWIGLU 0
+#define ORC_ACT_SWIGLU_OAI 1
+
+/* SwiGLU-OAI ("Tracing the bottleneck: optimising MiniMax M3 on AMD Instinct
+ * MI355X", correctness passage: the model's SwiGLU-OAI parameters are passed
+ * into the MoE; the page gives neither the formula nor the values).  Reading:
+ * the gate is clamped above at `limit`, the up projection to [-limit, limit],
+ * h = g * sigmoid(alpha * g) * (u + 1).  Parity unpinned beyond the special
+ * cases the tests reduce to textbook functions (limit = 0; alpha = 1 with no
+ * clamp). */
+double orc_swiglu_oai(double g, double u, double alpha, double limit) {
+  if (g > limit) g = limit;
+  if (u > limit) u = limit;
+  if (u < -limit) u = -limit;
+  return g / (1.0 + exp(-alpha * g)) * (u + 1.0);
+}
+
 /* Decode an MX matrix [rows, K] (codes in `fmt`, E8M0 scales per 32) to fp64. */
 static void decode_matrix(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t K,
                           int fmt, double* out) {
@@ -301,7 +320,8 @@ static void decode_matrix(const uint8_t* codes, const uint8_t* scales, int64_t r
 
 /*
  * The expert layer on already-quantised activations.
- *   act_codes/act_scales: MXFP8 activations [T, H], [T, H/32].
+ *   act_codes/act_scales: MX activations in `act_fmt` ([T, H] E4M3 codes or
+ *     [T, H/2] packed E2M1 codes), scales [T, H/32].
  *   ids/topk_w: router output [T, k].
  *   w1c/w1s[e], w2c/w2s[e], e = 0..E (E = shared): canonical MX weights,
  *     W1 [2I, H] (rows 0..I-1 gate, I..2I-1 up), W2 [H, I]; a NULL entry is
@@ -309,21 +329,33 @@ static void decode_matrix(const uint8_t* codes, const uint8_t* scales, int64_t r
  *   tokens[n_tokens]: distinct token indices to evaluate (NULL = all T).
  *   out[n_tokens, H]: fp64 result, rows in the order of `tokens`.
  *   out_noq (optional): the same layer with h left unquantised.
- *   h_codes/h_scales (optional): MXFP8 h per slot id t*(k+1)+j, [T*(k+1), I]
- *     and [T*(k+1), I/32]; rows of tokens not requested are left untouched.
+ *   h_codes/h_scales (optional): h per slot id t*(k+1)+j in `h_fmt`,
+ *     [T*(k+1), I] (E4M3) or [T*(k+1), I/2] (E2M1) and [T*(k+1), I/32]; rows of
+ *     tokens not requested are left untouched.
+ *   act: ORC_ACT_SWIGLU (h = silu(g) * u) or ORC_ACT_SWIGLU_OAI with `alpha`
+ *     and `limit` (orc_swiglu_oai).
+ *   h_fmt: the MX element format h is re-quantised to (E4M3; E2M1 for the
+ *     variant with MXFP4 activations, whose both MMA operands are E2M1).
  * Experts are visited in ascending order (shared last) and each token's
  * contributions are added in that order.
  */
-int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T, int H, int I,
-                     int E, int k, const int32_t* ids, const double* topk_w,
-                     const uint8_t* const* w1c, const uint8_t* const* w1s,
-                     const uint8_t* const* w2c, const uint8_t* const* w2s, int fmt,
-                     const int32_t* tokens, int n_tokens, double* out, double* out_noq,
-                     uint8_t* h_codes, uint8_t* h_scales) {
+int orc_expert_layer_ex(const uint8_t* act_codes, const uint8_t* act_scales, int T, int H, int I,
+                        int E, int k, const int32_t* ids, const double* topk_w,
+                        const uint8_t* const* w1c, const uint8_t* const* w1s,
+                        const uint8_t* const* w2c, const uint8_t* const* w2s, int fmt,
+                        const int32_t* tokens, int n_tokens, double* out, double* out_noq,
+                        uint8_t* h_codes, uint8_t* h_scales, int act, double alpha, double limit,
+                        int act_fmt, int h_fmt) {
   if (!act_codes || !act_scales || !ids || !topk_w || !w1c || !w1s || !w2c || !w2s || !out)
     return ORC_ERR_ARG;
   if (T < 0 || H <= 0 || I <= 0 || H % 32 || I % 32 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
   if (fmt != ORC_E4M3 && fmt != ORC_E2M1) return ORC_ERR_ARG;
+  if (act != ORC_ACT_SWIGLU && act != ORC_ACT_SWIGLU_OAI) return ORC_ERR_ARG;
+  if ((act_fmt != ORC_E4M3 && act_fmt != ORC_E2M1) || (h_fmt != ORC_E4M3 && h_fmt != ORC_E2M1)) return ORC_ERR_ARG;
+  /* row bytes of the activation and h codes: one byte per element (E4M3) or
+   * two elements per byte, element 2i in the low nibble (E2M1) */
+  const int64_t act_row = (act_fmt == ORC_E4M3) ? H : H / 2;
+  const int64_t h_row = (h_fmt == ORC_E4M3) ? I : I / 2;
   if (!tokens) n_tokens = T;
   int* row_of = (int*)malloc(sizeof(int) * (size_t)(T > 0 ? T : 1));
   double* xd = (double*)malloc(sizeof(double) * (size_t)n_tokens * H + 1);
@@ -346,9 +378,16 @@ int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T,
   }
   for (int r = 0; r < n_tokens; ++r) {
     int t = tokens ? tokens[r] : r;
-    for (int h = 0; h < H; ++h)
-      xd[(int64_t)r * H + h] =
-          orc_decode_e4m3(act_codes[(int64_t)t * H + h]) * orc_decode_e8m0(act_scales[(int64_t)t * (H / 32) + h / 32]);
+    for (int h = 0; h < H; ++h) {
+      double xv;
+      if (act_fmt == ORC_E4M3) {
+        xv = orc_decode_e4m3(act_codes[(int64_t)t * H + h]);
+      } else {
+        uint8_t byte = act_codes[(int64_t)t * act_row + h / 2];
+        xv = orc_decode_e2m1((h % 2 == 0) ? (byte & 0xF) : (byte >> 4));
+      }
+      xd[(int64_t)r * H + h] = xv * orc_decode_e8m0(act_scales[(int64_t)t * (H / 32) + h / 32]);
+    }
   }
   for (int64_t i = 0; i < (int64_t)n_tokens * H; ++i) out[i] = 0.0;
   if (out_noq)
@@ -393,19 +432,24 @@ int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T,
           g += x[h] * w1d[(int64_t)i * H + h];
           u += x[h] * w1d[(int64_t)(I + i) * H + h];
         }
-        hv[i] = silu(g) * u;
+        if (act == ORC_ACT_SWIGLU_OAI) hv[i] = orc_swiglu_oai(g, u, alpha, limit);
+        else hv[i] = silu(g) * u;
       }
-      /* re-quantise h to MXFP8 per 32 along I */
+      /* re-quantise h per 32 along I (MXFP8, or MXFP4 with FP4 activations) */
       uint8_t* hs = hc + I;
-      int qst = orc_quantize_rows(hv, 1, I, ORC_E4M3, hc, hs);
+      int qst = orc_quantize_rows(hv, 1, I, h_fmt, hc, hs);
       if (qst) {
 #pragma omp atomic write
         bad = qst;
       }
-      for (int i = 0; i < I; ++i) hq[i] = orc_decode_e4m3(hc[i]) * orc_decode_e8m0(hs[i / 32]);
+      for (int i = 0; i < I; ++i) {
+        double hcv = (h_fmt == ORC_E4M3) ? orc_decode_e4m3(hc[i])
+                                          : orc_decode_e2m1((i % 2 == 0) ? (hc[i / 2] & 0xF) : (hc[i / 2] >> 4));
+        hq[i] = hcv * orc_decode_e8m0(hs[i / 32]);
+      }
       if (h_codes && h_scales) {
         int64_t sid = (int64_t)t * (k + 1) + slot_j[si];
-        memcpy(h_codes + sid * I, hc, (size_t)I);
+        memcpy(h_codes + sid * h_row, hc, (size_t)h_row);
         memcpy(h_scales + sid * (I / 32), hs, (size_t)I / 32);
       }
       for (int o = 0; o < H; ++o) {
@@ -436,6 +480,19 @@ int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T,
 done:
   free(row_of); free(xd); free(w1d); free(w2d); free(slot_tok); free(slot_j); free(ybuf); free(ybuf_noq);
   return st;
+}
+
+/* The expert layer with the defaults: standard SwiGLU, MXFP8 activations and
+ * MXFP8 h (see orc_expert_layer_ex). */
+int orc_expert_layer(const uint8_t* act_codes, const uint8_t* act_scales, int T, int H, int I,
+                     int E, int k, const int32_t* ids, const double* topk_w,
+                     const uint8_t* const* w1c, const uint8_t* const* w1s,
+                     const uint8_t* const* w2c, const uint8_t* const* w2s, int fmt,
+                     const int32_t* tokens, int n_tokens, double* out, double* out_noq,
+                     uint8_t* h_codes, uint8_t* h_scales) {
+  return orc_expert_layer_ex(act_codes, act_scales, T, H, I, E, k, ids, topk_w, w1c, w1s, w2c, w2s, fmt,
+                             tokens, n_tokens, out, out_noq, h_codes, h_scales, ORC_ACT_SWIGLU, 1.0,
+                             INFINITY, ORC_E4M3, ORC_E4M3);
 }
 
 /* Number of OpenMP threads the oracle's parallel loops use from now on (the

@@ -83,8 +83,17 @@ MUTANTS = [
     ("gate_weight_transposed", "g += x[h] * w1d[(int64_t)i * H + h];", "g += x[h] * w1d[(int64_t)h * I + i];"),
     ("down_weight_transposed", "y += hq[i] * w2d[(int64_t)o * I + i];", "y += hq[i] * w2d[(int64_t)i * H + o];"),
     ("h_not_requantised", "y += hq[i] * w2d", "y += hv[i] * w2d"),
-    ("h_requantised_in_weight_format", "orc_quantize_rows(hv, 1, I, ORC_E4M3, hc, hs)",
+    ("h_requantised_in_weight_format", "orc_quantize_rows(hv, 1, I, h_fmt, hc, hs)",
      "orc_quantize_rows(hv, 1, I, fmt, hc, hs)"),
+    # SwiGLU-OAI and the MXFP4-activation variant
+    ("oai_gate_clamped_below_too", "  if (g > limit) g = limit;\n", "  if (g > limit) g = limit;\n  if (g < -limit) g = -limit;\n"),
+    ("oai_up_not_clamped", "  if (u > limit) u = limit;\n  if (u < -limit) u = -limit;\n", ""),
+    ("oai_no_plus_one", "return g / (1.0 + exp(-alpha * g)) * (u + 1.0);", "return g / (1.0 + exp(-alpha * g)) * u;"),
+    ("oai_alpha_outside_sigmoid", "return g / (1.0 + exp(-alpha * g)) * (u + 1.0);",
+     "return alpha * g / (1.0 + exp(-g)) * (u + 1.0);"),
+    ("fp4_act_high_nibble_first", "xv = orc_decode_e2m1((h % 2 == 0) ? (byte & 0xF) : (byte >> 4));",
+     "xv = orc_decode_e2m1((h % 2 == 1) ? (byte & 0xF) : (byte >> 4));"),
+    ("fp4_h_decoded_as_e4m3", "double hcv = (h_fmt == ORC_E4M3) ?", "double hcv = 1 ?"),
     ("router_weight_dropped", "double wt = (j == k) ? 1.0 : topk_w[(int64_t)t * k + j];", "double wt = 1.0;"),
     ("shared_takes_first_router_weight", "double wt = (j == k) ? 1.0 : topk_w[(int64_t)t * k + j];",
      "double wt = (j == k) ? topk_w[(int64_t)t * k] : topk_w[(int64_t)t * k + j];"),

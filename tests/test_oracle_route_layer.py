@@ -66,7 +66,7 @@ def test_permute_invariants_and_stable_sort(orc, T, E, k):
 
 
 # ---------------------------------------------------------------- expert layer
-def _random_layer(orc, rng, T, H, I, E, k, fmt, std=0.05):
+def _random_layer(orc, rng, T, H, I, E, k, fmt, std=0.05, act_fmt=None):
     w1c, w1s, w2c, w2s = [], [], [], []
     for _ in range(E + 1):
         c, s = orc.quantize_rows(rng.standard_normal((2 * I, H)) * std, fmt)
@@ -74,18 +74,23 @@ def _random_layer(orc, rng, T, H, I, E, k, fmt, std=0.05):
         c, s = orc.quantize_rows(rng.standard_normal((H, I)) * std, fmt)
         w2c.append(c), w2s.append(s)
     x = rng.standard_normal((T, H))
-    act_c, act_s = orc.quantize_rows(x, orc.E4M3)
+    act_c, act_s = orc.quantize_rows(x, orc.E4M3 if act_fmt is None else act_fmt)
     l = rng.standard_normal((T, E)).astype(np.float32)
     ids, w = orc.route_topk(l, k)
     return act_c, act_s, ids, w, w1c, w1s, w2c, w2s
 
 
-def _numpy_layer(orc, act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, requant=True, skip_shared=False):
-    """Per-token loops with no permutation: BLAS matmuls, scipy's logistic."""
-    T, H = act_c.shape
+def _numpy_layer(orc, act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, requant=True, skip_shared=False,
+                 oai=None, act_fmt=None):
+    """Per-token loops with no permutation: BLAS matmuls, scipy's logistic.
+    oai = (alpha, limit): the SwiGLU-OAI activation; act_fmt: the MX format of
+    the activations and of h (default MXFP8)."""
+    act_fmt = orc.E4M3 if act_fmt is None else act_fmt
+    T = act_c.shape[0]
+    H = act_s.shape[1] * 32
     E = len(w1c) - 1
     k = ids.shape[1]
-    x = orc.decode_matrix(act_c, act_s, orc.E4M3)
+    x = orc.decode_matrix(act_c, act_s, act_fmt)
     out = np.zeros((T, H))
     dec1 = [orc.decode_matrix(w1c[e], w1s[e], fmt) for e in range(E + 1)]
     dec2 = [orc.decode_matrix(w2c[e], w2s[e], fmt) for e in range(E + 1)]
@@ -96,10 +101,15 @@ def _numpy_layer(orc, act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, requant=
         for e, wt in pairs:
             g = dec1[e][:I] @ x[t]
             u = dec1[e][I:] @ x[t]
-            h = g * sps.expit(g) * u
+            if oai is None:
+                h = g * sps.expit(g) * u
+            else:
+                alpha, limit = oai
+                gc, uc = np.minimum(g, limit), np.clip(u, -limit, limit)
+                h = gc * sps.expit(alpha * gc) * (uc + 1.0)
             if requant:
-                hc, hs = orc.quantize_rows(h[None, :], orc.E4M3)
-                h = orc.decode_matrix(hc, hs, orc.E4M3)[0]
+                hc, hs = orc.quantize_rows(h[None, :], act_fmt)
+                h = orc.decode_matrix(hc, hs, act_fmt)[0]
             out[t] += wt * (dec2[e] @ h)
     return out
 
@@ -121,6 +131,56 @@ def test_layer_matches_numpy_per_token_loops(orc, fmt_name, T, H, I, E, k):
     # token subset gives the same rows
     sub = orc.expert_layer(act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, tokens=[4, 0, 2])
     assert np.array_equal(sub["out"], res["out"][[4, 0, 2]])
+
+
+def test_swiglu_oai_special_cases(orc):
+    """SwiGLU-OAI against textbook functions where it reduces to one: a clamp
+    limit of 0 leaves silu of the non-positive part of the gate (the up
+    projection clamps to 0 and enters as 0 + 1); alpha = 1 with no clamp is
+    silu(g) * (u + 1); a steep sigmoid is relu(g) * (u + 1); clamping caps the
+    gate from above only and the up projection on both sides."""
+    g = np.linspace(-6, 6, 49)
+    u = np.linspace(3, -3, 49)
+    silu = g * sps.expit(g)
+    assert np.allclose(orc.swiglu_oai(g, u, 1.0, 0.0), np.where(g < 0, silu, 0.0), rtol=1e-14, atol=1e-15)
+    assert np.allclose(orc.swiglu_oai(g, u, 1.0, np.inf), silu * (u + 1.0), rtol=1e-14, atol=1e-15)
+    steep = orc.swiglu_oai(g[np.abs(g) > 1], u[np.abs(g) > 1], 200.0, np.inf)
+    assert np.allclose(steep, np.maximum(g, 0)[np.abs(g) > 1] * (u[np.abs(g) > 1] + 1.0), rtol=1e-12, atol=1e-12)
+    # gate 10 and up -10 under a limit of 7: 7 * sigmoid(1.702 * 7) * (-7 + 1)
+    assert np.isclose(orc.swiglu_oai([10.0], [-10.0], 1.702, 7.0)[0], 7.0 * sps.expit(1.702 * 7.0) * -6.0, rtol=1e-14)
+    # a gate far below the limit is left alone
+    assert np.isclose(orc.swiglu_oai([-10.0], [0.5], 1.0, 7.0)[0], -10.0 * sps.expit(-10.0) * 1.5, rtol=1e-14)
+
+
+@pytest.mark.parametrize("variant", ["oai_e4m3", "swiglu_e2m1_act", "oai_e2m1_act"])
+def test_layer_variants_match_numpy_per_token_loops(orc, variant):
+    """The layer with the SwiGLU-OAI activation and/or MXFP4 activations (and
+    MXFP4 h) against the per-token formulation, with a clamp limit small enough
+    that part of g and u is clamped."""
+    rng = np.random.default_rng(23)
+    T, H, I, E, k = 6, 64, 64, 5, 2
+    oai = (1.702, 0.15) if variant.startswith("oai") else None
+    fp4 = variant.endswith("e2m1_act")
+    fmt = orc.E2M1 if fp4 else orc.E4M3
+    act_fmt = orc.E2M1 if fp4 else orc.E4M3
+    act_c, act_s, ids, w, w1c, w1s, w2c, w2s = _random_layer(orc, rng, T, H, I, E, k, fmt, std=0.1, act_fmt=act_fmt)
+    kw = dict(act_fmt=act_fmt)
+    if oai:
+        kw.update(act=orc.ACT_SWIGLU_OAI, alpha=oai[0], limit=oai[1])
+    res = orc.expert_layer(act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, want_noq=True, want_h=True, **kw)
+    ref = _numpy_layer(orc, act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, oai=oai, act_fmt=act_fmt)
+    scale = np.sqrt(np.mean(ref ** 2))
+    assert scale > 0
+    assert np.max(np.abs(res["out"] - ref)) <= 1e-12 * scale
+    ref_noq = _numpy_layer(orc, act_c, act_s, ids, w, w1c, w1s, w2c, w2s, fmt, I, requant=False, oai=oai,
+                           act_fmt=act_fmt)
+    assert np.max(np.abs(res["out_noq"] - ref_noq)) <= 1e-12 * scale
+    assert res["h_codes"].shape[1] == (I // 2 if fp4 else I)
+    if oai:
+        # the clamp is active: some gate values exceed the limit
+        x = orc.decode_matrix(act_c, act_s, act_fmt)
+        g = x @ orc.decode_matrix(w1c[E], w1s[E], fmt)[:I].T
+        assert np.any(g > oai[1]) and np.any(g < oai[1])
 
 
 def test_folded_shared_expert_equals_separate_dense_mlp(orc):
