@@ -374,6 +374,51 @@ def run_reference(args, wl, rank, world):
 
 
 # ------------------------------------------------------------------ GPU arm
+def time_fused(layer, x, logits, out, steps, warmup, flush, stream, dev, opts=None):
+    """Mean us of moe_forward (or moe_forward_ex with `opts`) replayed from a
+    CUDA graph, L2 flushed between steps outside the events."""
+    for _ in range(warmup):
+        layer.forward(x, logits, out, opts=opts)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            layer.forward(x, logits, out, opts=opts)
+    stream.wait_stream(cap)
+    for _ in range(warmup):
+        flush.fill_(1)
+        graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return 1e3 * float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+
+def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us):
+    """The layer variants timed beside the default: the shared expert as its own
+    dense launches (the A/B of the folded table), and the SwiGLU-OAI epilogue."""
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    out = torch.empty(wl.T, wl.H, dtype=torch.float32, device=dev)
+    dense = mx.layer_opts(shared="dense")
+    oai = mx.layer_opts("swiglu_oai", alpha=1.702, limit=7.0)
+    dense_us = time_fused(layer, x, logits, out, args.steps, args.warmup, flush, stream, dev, dense)
+    oai_us = time_fused(layer, x, logits, out, args.steps, args.warmup, flush, stream, dev, oai)
+    if mx.moe_get_status(layer.workspace(wl.T)):
+        raise RuntimeError(f"{wl.name}: device status error in a layer variant")
+    return {"shared_expert": {"folded_us": folded_us, "dense_us": dense_us,
+                              "folded_speedup": dense_us / folded_us,
+                              "dense_launches": mx.moe_forward_launches_ex(wl.T, wl.H, wl.I, wl.E, wl.k, layer.fmt, dense)},
+            "swiglu_oai": {"us_per_layer": oai_us, "alpha": 1.702, "limit": 7.0}}
+
+
 def measure_workload(args, wl, dev, world, clk, with_cpu):
     """Times one workload; returns its entry (headline keys included)."""
     from block_scaled_mx_gb300 import mxmoe as mx
@@ -503,6 +548,7 @@ def measure_workload(args, wl, dev, world, clk, with_cpu):
     e2e = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
     if mx.moe_get_status(layer.workspace(T)):
         raise RuntimeError(f"{wl.name}: device status error in moe_forward")
+    variants = measure_variants(args, layer, wl, x, logits, flush, stream, dev, ms * 1e3)
 
     pk = peaks()
     gemm1_ms = float(per[:, 3].mean())
@@ -548,6 +594,7 @@ def measure_workload(args, wl, dev, world, clk, with_cpu):
         "clocks": clk.summary((t_wall0, t_wall1)),
         "gpu_launches": (fused_launches + step_launches) * args.steps,
         "wall_s_timed": t_wall1 - t_wall0,
+        "variants": variants,
     }
     del layer, flush
     torch.cuda.empty_cache()
@@ -613,6 +660,7 @@ def run_gpu(args, rank, world, local):
         "clocks": head["clocks"],
         "gpu_launches": head["gpu_launches"],
         "wall_s_timed": head["wall_s_timed"],
+        "variants": head["variants"],
         "sms": torch.cuda.get_device_properties(dev).multi_processor_count,
         "build": {"stamp": mx.mx_build_stamp(), "compiled_in_this_run": bool(B.LAST_BUILD.get("compiled"))},
         "workloads": {n: dict(e, config=config_of(W.WORKLOADS[n], world)) for n, e in entries.items()},

@@ -75,11 +75,11 @@ size_t gather_bytes(int T, int H, int E, int k) {
 // the prologue; the chunked permutation when the prologue cannot permute
 // (count + scatter, or count alone for one chunk); the row gather of the wide
 // schedule; the two grouped GEMMs.
-int forward_launches(int T, int E, int k) {
+int forward_launches(int T, int E, int k, bool dense_shared = false) {
   const bool wide = wide_schedule(T, E, k);
   const bool fused = T <= kPermuteChunk && !wide;
   const int nchunks = (T + kPermuteChunk - 1) / kPermuteChunk;
-  return 1 + (fused ? 0 : (nchunks > 1 ? 2 : 1)) + (wide ? 1 : 0) + 2;
+  return 1 + (fused ? 0 : (nchunks > 1 ? 2 : 1)) + (wide ? 1 : 0) + (dense_shared ? 4 : 2);
 }
 
 // moe_forward workspace carve (status word first, shared with the permutation
@@ -125,17 +125,57 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
   return f;
 }
 
+// The layer options, checked and with defaults filled in.
+struct LayerOpts {
+  int act = MX_ACT_SWIGLU;
+  float alpha = 1.0f, limit = 0.0f;
+  int shared = MX_SHARED_FOLDED;
+  int act_fmt = MX_E4M3;
+};
+
+int read_opts(const mx_layer_opts* o, LayerOpts* out) {
+  LayerOpts r;
+  if (o) {
+    if (o->activation != MX_ACT_SWIGLU && o->activation != MX_ACT_SWIGLU_OAI) return MX_ERR_INVALID_ARG;
+    if (o->shared_expert != MX_SHARED_FOLDED && o->shared_expert != MX_SHARED_DENSE) return MX_ERR_INVALID_ARG;
+    if (o->act_fmt != MX_E4M3 && o->act_fmt != MX_E2M1) return MX_ERR_INVALID_ARG;
+    if (o->activation == MX_ACT_SWIGLU_OAI && !(o->limit > 0.0f && o->limit <= 3.0e38f && o->alpha == o->alpha &&
+                                                 o->alpha > -3.0e38f && o->alpha < 3.0e38f))
+      return MX_ERR_INVALID_ARG;
+    r.act = o->activation;
+    r.alpha = o->alpha;
+    r.limit = o->limit;
+    r.shared = o->shared_expert;
+    r.act_fmt = o->act_fmt;
+  }
+  if (r.act_fmt != MX_E4M3) return MX_ERR_UNSUPPORTED;
+  *out = r;
+  return MX_OK;
+}
+
+// The experts one grouped-GEMM launch covers: n table experts from e_base
+// (n = 0: all E + 1).
+struct Window {
+  int n = 0, e_base = 0;
+};
+
 int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const void* w1_prep, int fmt, int T, int H, int I, int E,
               int k, uint8_t* h_codes, uint8_t* h_scales, int* status, uint8_t* act_sorted,
-              cudaStream_t s, int pdl = 0) {
+              cudaStream_t s, int pdl = 0, const LayerOpts& lo = LayerOpts(), Window win = Window(),
+              bool gather_rows = true) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
   a.bn = choose_bn(T, E, k, 0);
   a.gather4 = a.bn <= 64 ? 1 : 0;
   a.pdl = a.gather4 ? pdl : 0;
-  if (!a.gather4) {
+  a.act = lo.act;
+  a.alpha = lo.alpha;
+  a.limit = lo.limit;
+  a.n_exp = win.n;
+  a.e_base = win.e_base;
+  if (!a.gather4 && gather_rows) {
     if (launch_gather_rows(act_codes, T, H, sorted_slot, k, n_rows, act_sorted, status, s) != cudaSuccess)
       return MX_ERR_CUDA;
   }
@@ -150,7 +190,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.b_codes = a.gather4 ? act_codes : act_sorted;
   a.n_rows = n_rows;
   a.b_scales = act_scales;
-  a.offsets = offsets;
+  a.offsets = offsets + win.e_base;
   a.sorted_slot = sorted_slot;
   a.h_codes = h_codes;
   a.h_scales = h_scales;
@@ -162,7 +202,8 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
 
 int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const float* topk_w, const void* w2_prep, int fmt, int T,
-              int H, int I, int E, int k, float* out, int* status, cudaStream_t s, int pdl = 0) {
+              int H, int I, int E, int k, float* out, int* status, cudaStream_t s, int pdl = 0,
+              Window win = Window()) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
@@ -177,7 +218,9 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.b_codes = h_codes;
   a.n_rows = n_rows;
   a.b_scales = h_scales;
-  a.offsets = offsets;
+  a.offsets = offsets + win.e_base;
+  a.n_exp = win.n;
+  a.e_base = win.e_base;
   a.sorted_slot = sorted_slot;
   a.topk_w = topk_w;
   a.out = out;
@@ -286,7 +329,20 @@ int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
                             const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
                             int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
                             uint8_t* h_scales, void* ws, size_t ws_bytes, mx_stream_t stream) {
-  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  return moe_grouped_gemm_swiglu_ex(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k,
+                                    h_codes, h_scales, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_grouped_gemm_swiglu_ex(const uint8_t* act_codes, const uint8_t* act_scales,
+                               const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
+                               int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
+                               uint8_t* h_scales, void* ws, size_t ws_bytes, const mx_layer_opts* opts,
+                               mx_stream_t stream) {
+  LayerOpts lo;
+  int st = read_opts(opts, &lo);
+  if (st != MX_OK) return st;
+  if (lo.shared != MX_SHARED_FOLDED) return MX_ERR_INVALID_ARG;
+  st = check_gemm_shape(T, H, I, E, k, fmt);
   if (st != MX_OK) return st;
   if (!offsets || !w1_prep || !ws) return MX_ERR_INVALID_ARG;
   if (T == 0) return MX_OK;
@@ -297,7 +353,7 @@ int moe_grouped_gemm_swiglu(const uint8_t* act_codes, const uint8_t* act_scales,
   if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(ws);
   return run_gemm1(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k, h_codes,
-                   h_scales, reinterpret_cast<int*>(w), w + al256(256), reinterpret_cast<cudaStream_t>(stream));
+                   h_scales, reinterpret_cast<int*>(w), w + al256(256), reinterpret_cast<cudaStream_t>(stream), 0, lo);
 }
 
 int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scales,
@@ -326,7 +382,16 @@ size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt) {
 int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
                 int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                 mx_stream_t stream) {
-  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  return moe_forward_ex(x_bf16, logits, w1_prep, w2_prep, fmt, T, H, I, E, k, out, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
+                   int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                   const mx_layer_opts* opts, mx_stream_t stream) {
+  LayerOpts lo;
+  int st = read_opts(opts, &lo);
+  if (st != MX_OK) return st;
+  st = check_gemm_shape(T, H, I, E, k, fmt);
   if (st != MX_OK) return st;
   if (T == 0) return MX_OK;
   if (!x_bf16 || !logits || !w1_prep || !w2_prep || !out || !ws) return MX_ERR_INVALID_ARG;
@@ -362,17 +427,44 @@ int moe_forward(const void* x_bf16, const float* logits, const void* w1_prep, co
   if (launch_prologue(pa, s) != cudaSuccess) return MX_ERR_CUDA;
   if (!fused && launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
     return MX_ERR_CUDA;
+  if (lo.shared == MX_SHARED_FOLDED) {
+    st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
+                   f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0, lo);
+    if (st != MX_OK) return st;
+    return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
+                     k, out, f.perm.status, s, 2);
+  }
+  // the shared expert as its own dense MLP: the routed experts' gate/up
+  // launch, the shared expert's gate/up launch over all T tokens, then the two
+  // down launches (the permutation's shared-slot segment feeds the dense
+  // launches, so the arithmetic is the folded layer's)
+  Window routed, shared;
+  routed.n = E;
+  shared.n = 1;
+  shared.e_base = E;
   st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0);
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0, lo, routed);
   if (st != MX_OK) return st;
-  return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
-                   k, out, f.perm.status, s, 2);
+  st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 2 : 0, lo, shared, false);
+  if (st != MX_OK) return st;
+  st = run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E, k, out,
+                 f.perm.status, s, 2, routed);
+  if (st != MX_OK) return st;
+  return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E, k, out,
+                   f.perm.status, s, 2, shared);
 }
 
 int moe_forward_launches(int T, int H, int I, int E, int k, int fmt) {
+  return moe_forward_launches_ex(T, H, I, E, k, fmt, nullptr);
+}
+
+int moe_forward_launches_ex(int T, int H, int I, int E, int k, int fmt, const mx_layer_opts* opts) {
+  LayerOpts lo;
+  if (read_opts(opts, &lo) != MX_OK) return -1;
   if (check_gemm_shape(T, H, I, E, k, fmt) != MX_OK) return -1;
   if (T == 0) return 0;
-  return forward_launches(T, E, k);
+  return forward_launches(T, E, k, lo.shared == MX_SHARED_DENSE);
 }
 
 int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {

@@ -63,6 +63,9 @@ constexpr int kMaxDevices = 64;
 
 struct GemmParams {
   int epi, afmt, T, H, I, E, k;
+  int n_exp, e_base;  // this launch covers n_exp experts, table experts e_base .. e_base + n_exp - 1
+  int act;            // gate/up epilogue: 0 SwiGLU, 1 SwiGLU-OAI
+  float alpha, limit; // SwiGLU-OAI: sigmoid slope, clamp limit
   int K, NK, NM, RB;
   int MG;  // weight tiles per tile group: groups of MG weight tiles (of every expert and
            // token tile) run one after the other, so the down GEMM's combine targets
@@ -233,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared sh;
   sh.base = base;
   sh.offs = reinterpret_cast<int*>(base + p.off_meta);
-  sh.prefix = sh.offs + (p.E + 2);
+  sh.prefix = sh.offs + (p.n_exp + 1);
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + p.off_bar);
   sh.full = bars;
   sh.empty = bars + S;
@@ -255,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up that needs nothing from the previous grid (barriers, tensor
   // memory) runs before waiting on it; then the expert offsets, per-expert
   // tile counts and their prefix
-  const int E1 = p.E + 1;
+  const int E1 = p.n_exp;  // experts of this launch
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       // a stage is full when its TMA bytes have landed (producer: 1 arrival
@@ -350,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = unit0; t < total && ok; t += unit_step) {
-      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
       const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       // a pair's MMA takes token rows [0, N/2) from rank 0 and [N/2, N) from
       // rank 1, N the tile's rows rounded up to 16
@@ -388,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
             // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
             // the TMA fills zeros and still counts the whole box)
-            const int blk0 = (tl.e * NK + kc) * p.RB + 2 * m;
+            const int blk0 = ((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m;
             tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
           }
         }
@@ -469,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kM = PAIR ? 256u : 128u;
       bool ok = true;
       for (int t = unit0; t < total && ok; t += unit_step) {
-        const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+        const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
         const int m = PAIR ? 2 * tl.m : tl.m;   // a pair's tiles both have two row blocks
         const bool two = p.epi == 0 || (2 * m + 1 < p.RB);
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
@@ -557,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = unit0; t < total && ok; t += unit_step) {
-      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
       const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       const bool two = 2 * m + 1 < p.RB;
       // rows 32j + lane of this tile: the word offset of their scale rows
@@ -587,14 +590,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sft = tid - kWarpSf0 * 32;
         for (int i = sft; i < NK * lines; i += 128) {
           const int kc = i / lines, line = i - kc * lines;
-          const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * m) * 32;
+          const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m) * 32;
           prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
         }
       }
       auto load = [&](ScaleBuf& b, int kc) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bsc + roww[j] + kc) : 0x7F7F7F7Fu;
-        const uint4* blk = wsc + static_cast<size_t>((tl.e * NK + kc) * p.RB + 2 * m) * 32;
+        const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m) * 32;
         b.a0 = __ldg(blk + lane);
         b.a1 = two ? __ldg(blk + 32 + lane) : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       };
@@ -671,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
     for (int t = unit0; t < total; t += unit_step) {
-      const Tile tl = decode_tile(t, sh, p.E, p.MG, p.bn, per_group);
+      const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
       const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       ab = ab_next;
       aph = aph_next;
@@ -690,6 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int I = p.I, I32 = p.I / 32;
         uint8_t* const h_codes = p.h_codes;
         uint8_t* const h_scales = p.h_scales;
+        const bool act_oai = p.act != 0;
+        const float alpha = p.alpha, limit = p.limit;
         // 8 columns at a time, each step over all 8 so that the per-column
         // chains (SwiGLU, warp amax, exponent, encode) overlap; the tensor-
         // memory loads of the warp's next 8 columns are in flight while the
@@ -698,9 +703,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) {
             // silu(g) * u with the fast reciprocal: h is re-quantised to 3
-            // mantissa bits right after, far coarser than its 2-ulp error
-            const float gv = __uint_as_float(g[cc]);
-            const float hv = __fdividef(gv, 1.0f + __expf(-gv)) * __uint_as_float(u[cc]);
+            // mantissa bits right after, far coarser than its 2-ulp error.
+            // SwiGLU-OAI: the gate clamped above at `limit`, the up projection
+            // to [-limit, limit], h = g * sigmoid(alpha * g) * (u + 1).
+            float gv = __uint_as_float(g[cc]);
+            float uv = __uint_as_float(u[cc]);
+            float sl = 1.0f;
+            if (act_oai) {
+              gv = fminf(gv, limit);
+              uv = fminf(fmaxf(uv, -limit), limit) + 1.0f;
+              sl = alpha;
+            }
+            const float hv = __fdividef(gv, 1.0f + __expf(-sl * gv)) * uv;
             g[cc] = __float_as_uint(hv);
             u[cc] = __float_as_uint(hv) & 0x7FFFFFFFu;
           }
@@ -901,6 +915,11 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.I = a.I;
   p.E = a.E;
   p.k = a.k;
+  p.n_exp = a.n_exp > 0 ? a.n_exp : a.E + 1;
+  p.e_base = a.e_base;
+  p.act = a.act;
+  p.alpha = a.alpha;
+  p.limit = a.limit;
   const int rows = a.epi == 0 ? 2 * a.I : a.H;
   p.K = a.epi == 0 ? a.H : a.I;
   p.NK = p.K / 128;
@@ -943,7 +962,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
 
   // shared memory and tensor memory plan for `kps` 128-wide K chunks per
   // pipeline stage: returns the stage count (0 if fewer than two fit)
-  const uint32_t meta_bytes = (static_cast<uint32_t>(a.E + 2) * 8u + 127u) & ~127u;
+  const uint32_t meta_bytes = (static_cast<uint32_t>(p.n_exp + 1) * 8u + 127u) & ~127u;
   int dev = 0;
   cudaGetDevice(&dev);
   int max_smem = 0;
@@ -1050,7 +1069,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   // upper bound on work units: NM * sum_e ceil(count_e / bn) <= NM * (E + 1 + rows / bn)
   const long long bound =
-      static_cast<long long>(p.NM) * (a.E + 1 + (a.n_rows + p.bn - 1) / p.bn);
+      static_cast<long long>(p.NM) * (p.n_exp + (a.n_rows + p.bn - 1) / p.bn);
   int units = sm_count_gemm() / (pair ? 2 : 1);
   if (bound < units) units = static_cast<int>(bound > 0 ? bound : 1);
   const int grid = units * (pair ? 2 : 1);

@@ -102,6 +102,12 @@ struct GemmArgs {
   // run as clusters of two CTAs with the pair MMA (M = 256 over two SMs; each
   // SM loads half of the token rows); needs pair_supported()
   int pair;
+  // expert window: this launch covers n_exp experts (0: all E + 1), table
+  // experts e_base .. e_base + n_exp - 1; `offsets` then points at entry e_base
+  int n_exp, e_base;
+  // gate/up epilogue activation: 0 SwiGLU, 1 SwiGLU-OAI with alpha and limit
+  int act;
+  float alpha, limit;
 };
 bool pair_supported(const GemmArgs& a);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);

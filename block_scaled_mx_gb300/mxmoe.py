@@ -28,6 +28,23 @@ MX_ERR_DEVICE_ARG = 7
 MX_E4M3 = 0
 MX_E2M1 = 1
 FORMATS = {"e4m3": MX_E4M3, "e2m1": MX_E2M1}
+MX_ACT_SWIGLU = 0
+MX_ACT_SWIGLU_OAI = 1
+MX_SHARED_FOLDED = 0
+MX_SHARED_DENSE = 1
+
+
+class LayerOpts(ctypes.Structure):
+    """mx_layer_opts of include/mxmoe.h (field order and types as declared)."""
+    _fields_ = [("activation", ctypes.c_int), ("alpha", ctypes.c_float), ("limit", ctypes.c_float),
+                ("shared_expert", ctypes.c_int), ("act_fmt", ctypes.c_int)]
+
+
+def layer_opts(activation="swiglu", alpha=1.0, limit=7.0, shared="folded", act_fmt="e4m3") -> LayerOpts:
+    """Options from names: activation "swiglu" | "swiglu_oai", shared "folded" | "dense"."""
+    return LayerOpts({"swiglu": MX_ACT_SWIGLU, "swiglu_oai": MX_ACT_SWIGLU_OAI}[activation], float(alpha),
+                     float(limit), {"folded": MX_SHARED_FOLDED, "dense": MX_SHARED_DENSE}[shared],
+                     FORMATS[act_fmt] if isinstance(act_fmt, str) else int(act_fmt))
 
 # every entry point of the C ABI: name -> (restype, argtypes)
 _P, _I, _I64, _SZ, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_uint64
@@ -46,6 +63,9 @@ SIGNATURES = {
     "moe_grouped_gemm_down_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_forward_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
+    "moe_grouped_gemm_swiglu_ex": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P, _P]),
+    "moe_forward_launches_ex": (_I, [_I, _I, _I, _I, _I, _I, _P]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_get_status": (_I, [_P, _P, _P]),
     "mx_debug_set_wait_limit_ns": (None, [_U64]),
@@ -174,6 +194,18 @@ def moe_grouped_gemm_swiglu(act_codes, act_scales, offsets, sorted_slot, w1_prep
            "moe_grouped_gemm_swiglu")
 
 
+def _opts_ptr(opts):
+    return None if opts is None else ctypes.addressof(opts)
+
+
+def moe_grouped_gemm_swiglu_ex(act_codes, act_scales, offsets, sorted_slot, w1_prep, fmt, T, H, I, E, k, h_codes,
+                               h_scales, ws, opts=None, stream=None):
+    _check(lib().moe_grouped_gemm_swiglu_ex(_ptr(act_codes), _ptr(act_scales), _ptr(offsets), _ptr(sorted_slot),
+                                            _ptr(w1_prep), _fmt(fmt), T, H, I, E, k, _ptr(h_codes), _ptr(h_scales),
+                                            _ptr(ws), ws.numel() * ws.element_size(), _opts_ptr(opts),
+                                            _stream(stream)), "moe_grouped_gemm_swiglu_ex")
+
+
 def moe_grouped_gemm_down_combine(h_codes, h_scales, offsets, sorted_slot, topk_w, w2_prep, fmt, T, H, I, E, k,
                                   out, ws, stream=None):
     _check(lib().moe_grouped_gemm_down_combine(_ptr(h_codes), _ptr(h_scales), _ptr(offsets), _ptr(sorted_slot),
@@ -196,6 +228,19 @@ def moe_forward(x, logits, w1_prep, w2_prep, fmt, I, k, out, ws, stream=None):
 def moe_forward_launches(T, H, I, E, k, fmt) -> int:
     """Kernel launches moe_forward enqueues for this shape (host only)."""
     return lib().moe_forward_launches(T, H, I, E, k, _fmt(fmt))
+
+
+def moe_forward_ex(x, logits, w1_prep, w2_prep, fmt, I, k, out, ws, opts=None, stream=None):
+    T, H = x.shape
+    E = logits.shape[1]
+    _check(lib().moe_forward_ex(_ptr(x), _ptr(logits), _ptr(w1_prep), _ptr(w2_prep), _fmt(fmt), T, H, I, E, k,
+                                _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _opts_ptr(opts),
+                                _stream(stream)), "moe_forward_ex")
+
+
+def moe_forward_launches_ex(T, H, I, E, k, fmt, opts=None) -> int:
+    """Kernel launches moe_forward_ex enqueues for this shape and these options (host only)."""
+    return lib().moe_forward_launches_ex(T, H, I, E, k, _fmt(fmt), _opts_ptr(opts))
 
 
 def moe_get_status(ws, stream=None) -> int:
@@ -240,9 +285,14 @@ class MoELayer:
             self._ws = alloc_workspace(need, device)
         return self._ws
 
-    def forward(self, x, logits, out=None, stream=None) -> torch.Tensor:
+    def forward(self, x, logits, out=None, stream=None, opts: Optional[LayerOpts] = None) -> torch.Tensor:
         T = x.shape[0]
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.float32, device=x.device)
-        moe_forward(x, logits, self.w1, self.w2, self.fmt, self.I, self.k, out, self.workspace(T, x.device), stream)
+        if opts is None:
+            moe_forward(x, logits, self.w1, self.w2, self.fmt, self.I, self.k, out, self.workspace(T, x.device),
+                        stream)
+        else:
+            moe_forward_ex(x, logits, self.w1, self.w2, self.fmt, self.I, self.k, out, self.workspace(T, x.device),
+                           opts, stream)
         return out

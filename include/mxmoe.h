@@ -228,6 +228,52 @@ MX_API int moe_forward(const void* x_bf16, const float* logits, const void* w1_p
  * -1 for a shape moe_forward rejects, 0 for T = 0). */
 MX_API int moe_forward_launches(int T, int H, int I, int E, int k, int fmt);
 
+/* ---- layer variants ---- */
+#define MX_ACT_SWIGLU 0      /* h = silu(g) * u */
+#define MX_ACT_SWIGLU_OAI 1  /* h = g' * sigmoid(alpha * g') * (u' + 1), g' = min(g, limit), u' = clamp(u, +-limit) */
+#define MX_SHARED_FOLDED 0   /* shared expert as a routed-table slot every token selects */
+#define MX_SHARED_DENSE 1    /* shared expert as its own dense MLP launches */
+
+/* Options of the layer variants (a NULL pointer means the defaults: SwiGLU,
+ * folded shared expert, MXFP8 activations).
+ *  - activation: MX_ACT_SWIGLU or MX_ACT_SWIGLU_OAI.  SwiGLU-OAI follows the
+ *    MI355X page's correctness passage (the model's SwiGLU-OAI parameters are
+ *    passed into the MoE); the page gives no values, the caller does: alpha
+ *    (the sigmoid slope) and limit (> 0; the gate is clamped above at limit,
+ *    the up projection to [-limit, limit]).
+ *  - shared_expert: MX_SHARED_FOLDED (the MI355X page's Figure 4: one grouped
+ *    GEMM pair covers routed and shared experts) or MX_SHARED_DENSE (the path
+ *    that figure replaces: the shared expert runs as its own dense gate/up and
+ *    down launches after the routed ones; same arithmetic, two more launches).
+ *  - act_fmt: MX_E4M3 (MXFP8 activations and h); MX_E2M1 is reserved for
+ *    MXFP4 activations (MX_ERR_UNSUPPORTED where not built). */
+typedef struct mx_layer_opts {
+  int activation;
+  float alpha;
+  float limit;
+  int shared_expert;
+  int act_fmt;
+} mx_layer_opts;
+
+/* moe_forward with layer options (see mx_layer_opts); the workspace size is
+ * moe_workspace_size's.  Errors: as moe_forward, plus MX_ERR_INVALID_ARG for
+ * an unknown option value or a non-positive / non-finite limit. */
+MX_API int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep, const void* w2_prep,
+                          int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                          const mx_layer_opts* opts, mx_stream_t stream);
+
+/* moe_grouped_gemm_swiglu with layer options (the activation is used; the
+ * other fields must hold their defaults). */
+MX_API int moe_grouped_gemm_swiglu_ex(const uint8_t* act_codes, const uint8_t* act_scales,
+                                      const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
+                                      int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
+                                      uint8_t* h_scales, void* ws, size_t ws_bytes, const mx_layer_opts* opts,
+                                      mx_stream_t stream);
+
+/* Kernel launches moe_forward_ex enqueues for this shape and these options
+ * (host only; -1 for a rejected shape or option). */
+MX_API int moe_forward_launches_ex(int T, int H, int I, int E, int k, int fmt, const mx_layer_opts* opts);
+
 /* Copy the workspace status word to *host_status (synchronising `stream`) and
  * clear it.  0 = no device-side error; otherwise an MX_ERR_* code. */
 MX_API int moe_get_status(void* ws, mx_stream_t stream, int* host_status);

@@ -125,3 +125,26 @@ def test_forward_launch_count(L):
     assert L.moe_forward_launches(0, 256, 128, 8, 2, 0) == 0
     assert L.moe_forward_launches(16, 256, 100, 8, 2, 0) == -1
     assert L.moe_forward_launches(8192, 4096, 1536, 128, 8, 0) >= 3
+
+
+def test_layer_options_are_checked_on_the_host(L):
+    """mx_layer_opts: unknown values and a non-positive clamp limit are invalid
+    arguments; MXFP4 activations are not available through this call; the
+    dense shared-expert variant adds two launches."""
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    fake = ctypes.c_void_p(256)
+    bad_act = mx.LayerOpts(7, 1.0, 7.0, 0, 0)
+    bad_limit = mx.layer_opts("swiglu_oai", alpha=1.702, limit=0.0)
+    bad_shared = mx.LayerOpts(0, 1.0, 7.0, 3, 0)
+    for o in (bad_act, bad_limit, bad_shared):
+        assert L.moe_forward_ex(fake, fake, fake, fake, 0, 4, 256, 128, 8, 2, fake, fake, 1 << 30, ctypes.addressof(o),
+                                None) == mx.MX_ERR_INVALID_ARG
+        assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, ctypes.addressof(o)) == -1
+    fp4 = mx.layer_opts(act_fmt="e2m1")
+    assert L.moe_forward_ex(fake, fake, fake, fake, 1, 4, 256, 128, 8, 2, fake, fake, 1 << 30,
+                            ctypes.addressof(fp4), None) == mx.MX_ERR_UNSUPPORTED
+    dense = mx.layer_opts(shared="dense")
+    assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, ctypes.addressof(dense)) == 5
+    assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, None) == 3
+    assert mx.moe_forward_launches_ex(32, 4096, 1536, 128, 8, "e4m3", mx.layer_opts("swiglu_oai")) == 3

@@ -122,7 +122,7 @@ def test_permute_bitexact(T, E, k):
 
 
 # ------------------------------------------------------------------ layer
-def _steps(L):
+def _steps(L, opts=None):
     wl = L.wl
     T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
     d = "cuda"
@@ -141,8 +141,12 @@ def _steps(L):
     gws = mx.alloc_workspace(mx.moe_gemm_workspace_size(T, H, I, E, k))
     r["h_c"] = torch.empty(T * (k + 1), I, dtype=torch.uint8, device=d)
     r["h_s"] = torch.empty(T * (k + 1), I // 32, dtype=torch.uint8, device=d)
-    mx.moe_grouped_gemm_swiglu(r["act_c"], r["act_s"], r["offsets"], r["ss"], L.layer.w1, L.fmt, T, H, I, E, k,
-                               r["h_c"], r["h_s"], gws)
+    if opts is None:
+        mx.moe_grouped_gemm_swiglu(r["act_c"], r["act_s"], r["offsets"], r["ss"], L.layer.w1, L.fmt, T, H, I, E, k,
+                                   r["h_c"], r["h_s"], gws)
+    else:
+        mx.moe_grouped_gemm_swiglu_ex(r["act_c"], r["act_s"], r["offsets"], r["ss"], L.layer.w1, L.fmt, T, H, I, E,
+                                      k, r["h_c"], r["h_s"], gws, opts)
     r["out"] = torch.zeros(T, H, dtype=torch.float32, device=d)
     mx.moe_grouped_gemm_down_combine(r["h_c"], r["h_s"], r["offsets"], r["ss"], r["w"], L.layer.w2, L.fmt, T, H,
                                      I, E, k, r["out"], gws)
@@ -391,3 +395,66 @@ def test_pair_schedule_matches_single_cta(name, bn, monkeypatch):
         outs[pair] = out
     diff = (outs["1"] - outs["0"]).abs().max().item() / outs["0"].abs().max().item()
     assert diff < 1e-5, diff
+
+
+
+# ------------------------------------------------------------------ layer variants
+# SwiGLU-OAI: a clamp limit below the typical |g| of each shape (g ~ N(0, 0.02^2 H)
+# for these weights) so that the clamp acts; specverify with a limit that does not
+OAI_CASES = [("tiny", 0.2), ("decode_mxfp8", 0.7), ("ragged_e2m1", 0.3), ("wide_e4m3", 0.3),
+             ("specverify_mxfp4", 7.0)]
+
+
+@pytest.mark.parametrize("name,limit", OAI_CASES)
+def test_swiglu_oai_layer_parity(name, limit):
+    """The SwiGLU-OAI epilogue (caller alpha and clamp limit) against the
+    oracle's: h codes within the one-step rules, the layer output within the
+    output tolerance, through the step-wise call and the fused one."""
+    alpha = 1.702
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle.moe_forward(L.x_bits, L.logits_np, wl.k, L.o1c, L.o1s, L.o2c, L.o2s, L.fmt, wl.I, want_h=True,
+                             act=oracle.ACT_SWIGLU_OAI, alpha=alpha, limit=limit)
+    opts = mx.layer_opts("swiglu_oai", alpha=alpha, limit=limit)
+    r = _steps(L, opts)
+    assert r["status"] == (0, 0)
+    frac, hrel = _check_h(r, ref, wl.I)
+    print(f"h codes (SwiGLU-OAI) {name}: mismatch fraction {frac:.2e}, decoded rel L2 {hrel:.2e}")
+    assert frac < 0.005 and hrel < 0.01, (frac, hrel)
+    rel, mabs = out_errors(r["out"].double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    out = L.layer.forward(L.x, L.logits, opts=opts)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel2, mabs2 = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel2 <= OUT_REL_L2 and mabs2 <= OUT_MAX_ABS_OVER_RMS, (rel2, mabs2)
+    # the variant differs from the standard layer (the options reach the kernel)
+    std = oracle_forward(L)["out"]
+    assert np.linalg.norm(ref["out"] - std) > 10 * OUT_REL_L2 * np.linalg.norm(std)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_mxfp8", "specverify_mxfp4", "ragged_e4m3", "wide_e2m1",
+                                  "max_routing"])
+def test_dense_shared_expert_matches_folded(name):
+    """The shared expert run as its own dense launches (the path the folded
+    table replaces) gives the folded layer's output, and the oracle's."""
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    ref = oracle_forward(L)
+    folded = L.layer.forward(L.x, L.logits).clone()
+    dense = L.layer.forward(L.x, L.logits, opts=mx.layer_opts(shared="dense"))
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel, mabs = out_errors(dense.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    diff = (dense - folded).abs().max().item() / folded.abs().max().item()
+    assert diff < 1e-5, diff
+
+
+def test_dense_shared_expert_with_swiglu_oai():
+    wl = LAYER_CASES["ragged_e4m3"]
+    L = build_layer(wl)
+    ref = oracle.moe_forward(L.x_bits, L.logits_np, wl.k, L.o1c, L.o1s, L.o2c, L.o2s, L.fmt, wl.I,
+                             act=oracle.ACT_SWIGLU_OAI, alpha=1.5, limit=0.4)
+    out = L.layer.forward(L.x, L.logits, opts=mx.layer_opts("swiglu_oai", alpha=1.5, limit=0.4, shared="dense"))
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
