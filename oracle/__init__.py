@@ -62,6 +62,8 @@ def _bind(L):
                                    P, P, P, P]
     L.orc_expert_layer_ex.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, P, i32, P, i32,
                                       P, P, P, P, i32, ctypes.c_double, ctypes.c_double, i32, i32]
+    L.orc_router_logits.argtypes = [P, P, i32, i32, i32, P]
+    L.orc_route_topk_biased.argtypes = [P, P, i32, i32, i32, P, P]
     L.orc_swiglu_oai.restype = ctypes.c_double
     L.orc_swiglu_oai.argtypes = [ctypes.c_double] * 4
     L.orc_set_threads.argtypes = [i32]
@@ -201,6 +203,30 @@ def route_topk(logits: np.ndarray, k: int):
     ids = np.zeros((T, k), dtype=np.int32)
     w = np.zeros((T, k), dtype=np.float64)
     _check(lib().orc_route_topk(_ptr(l), T, E, k, _ptr(ids), _ptr(w)), "route_topk")
+    return ids, w
+
+
+def router_logits(x_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """bf16 activations [T, H] and bf16 router weights [E, H] (uint16 bit
+    patterns) -> fp64 logits [T, E] = x . w^T."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bits, dtype=np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    out = np.zeros((T, E), dtype=np.float64)
+    _check(lib().orc_router_logits(_ptr(x), _ptr(w), T, H, E, _ptr(out)), "router_logits")
+    return out
+
+
+def route_topk_biased(logits: np.ndarray, bias: Optional[np.ndarray], k: int):
+    """Top-k by the fp32 score logit + bias (lowest index on ties), weights =
+    softmax of the chosen experts' unbiased logits; bias None = route_topk."""
+    l = np.ascontiguousarray(logits, dtype=np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32)
+    T, E = l.shape
+    ids = np.zeros((T, k), dtype=np.int32)
+    w = np.zeros((T, k), dtype=np.float64)
+    _check(lib().orc_route_topk_biased(_ptr(l), _ptr(b), T, E, k, _ptr(ids), _ptr(w)), "route_topk_biased")
     return ids, w
 
 

@@ -252,6 +252,64 @@ int orc_route_topk(const float* logits, int T, int E, int k, int32_t* ids, doubl
   return ORC_OK;
 }
 
+/* Router GEMM (the step ahead of top-k): logits[t, e] = sum_h x[t, h] * w[e, h]
+ * for bf16 activations x [T, H] and bf16 router weights w [E, H], products and
+ * sums in fp64 (each bf16 product is exact in fp64).  The pages route tokens
+ * to experts by their router logits (the MI355X page, Figure 4 and the
+ * passage around it) without printing the router; a linear map of the hidden
+ * state is the plain reading. */
+int orc_router_logits(const uint16_t* x, const uint16_t* w, int T, int H, int E, double* logits) {
+  if (!x || !w || !logits || T < 0 || H <= 0 || E <= 0) return ORC_ERR_ARG;
+  for (int t = 0; t < T; ++t)
+    for (int e = 0; e < E; ++e) {
+      double acc = 0.0;
+      for (int h = 0; h < H; ++h)
+        acc += bf16_to_double(x[(int64_t)t * H + h]) * bf16_to_double(w[(int64_t)e * H + h]);
+      logits[(int64_t)t * E + e] = acc;
+    }
+  return ORC_OK;
+}
+
+/* Top-k with a load-balancing bias: experts are chosen by the fp32 score
+ * logit + bias[e] (the addition done in fp32, as the selection runs on the
+ * GPU), largest first, lowest index on ties; the weights are the softmax of
+ * the chosen experts' unbiased logits (fp64).  Reading: the bias steers which
+ * experts are chosen, not how much each contributes.  bias = NULL is
+ * orc_route_topk. */
+int orc_route_topk_biased(const float* logits, const float* bias, int T, int E, int k, int32_t* ids, double* w) {
+  if (!logits || !ids || !w || T < 0 || E <= 0 || k <= 0 || k > E) return ORC_ERR_ARG;
+  float* score = (float*)malloc(sizeof(float) * (size_t)E);
+  char* taken = (char*)malloc((size_t)E);
+  if (!score || !taken) { free(score); free(taken); return ORC_ERR_NOMEM; }
+  for (int t = 0; t < T; ++t) {
+    const float* l = logits + (int64_t)t * E;
+    for (int e = 0; e < E; ++e) {
+      if (!isfinite(l[e]) || (bias && !isfinite(bias[e]))) { free(score); free(taken); return ORC_ERR_NONFINITE; }
+      volatile float sum = l[e] + (bias ? bias[e] : 0.0f); /* one fp32 addition */
+      score[e] = sum;
+      taken[e] = 0;
+    }
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      for (int e = 0; e < E; ++e)
+        if (!taken[e] && (best < 0 || score[e] > score[best])) best = e;
+      taken[best] = 1;
+      ids[(int64_t)t * k + j] = best;
+    }
+    double lmax = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+      double v = (double)l[ids[(int64_t)t * k + j]];
+      if (v > lmax) lmax = v;
+    }
+    double den = 0.0;
+    for (int jj = 0; jj < k; ++jj) den += exp((double)l[ids[(int64_t)t * k + jj]] - lmax);
+    for (int jj = 0; jj < k; ++jj) w[(int64_t)t * k + jj] = exp((double)l[ids[(int64_t)t * k + jj]] - lmax) / den;
+  }
+  free(score);
+  free(taken);
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------------ permute */
 
 /* counts[e] = tokens routed to expert e (e < E), counts[E] = T (the shared

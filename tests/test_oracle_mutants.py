@@ -94,6 +94,13 @@ MUTANTS = [
     ("fp4_act_high_nibble_first", "xv = orc_decode_e2m1((h % 2 == 0) ? (byte & 0xF) : (byte >> 4));",
      "xv = orc_decode_e2m1((h % 2 == 1) ? (byte & 0xF) : (byte >> 4));"),
     ("fp4_h_decoded_as_e4m3", "double hcv = (h_fmt == ORC_E4M3) ?", "double hcv = 1 ?"),
+    # router GEMM and biased top-k
+    ("router_weight_transposed", "bf16_to_double(w[(int64_t)e * H + h])", "bf16_to_double(w[(int64_t)h * E + e])"),
+    ("router_drops_last_column", "      for (int h = 0; h < H; ++h)\n        acc +=", "      for (int h = 0; h < H - 1; ++h)\n        acc +="),
+    ("biased_weights_from_scores", "den += exp((double)l[ids[(int64_t)t * k + jj]] - lmax);\n    for (int jj = 0; jj < k; ++jj) w[(int64_t)t * k + jj] = exp((double)l[ids[(int64_t)t * k + jj]] - lmax) / den;",
+     "den += exp((double)score[ids[(int64_t)t * k + jj]] - lmax);\n    for (int jj = 0; jj < k; ++jj) w[(int64_t)t * k + jj] = exp((double)score[ids[(int64_t)t * k + jj]] - lmax) / den;"),
+    ("biased_ties_to_highest", "if (!taken[e] && (best < 0 || score[e] > score[best])) best = e;",
+     "if (!taken[e] && (best < 0 || score[e] >= score[best])) best = e;"),
     ("router_weight_dropped", "double wt = (j == k) ? 1.0 : topk_w[(int64_t)t * k + j];", "double wt = 1.0;"),
     ("shared_takes_first_router_weight", "double wt = (j == k) ? 1.0 : topk_w[(int64_t)t * k + j];",
      "double wt = (j == k) ? topk_w[(int64_t)t * k] : topk_w[(int64_t)t * k + j];"),

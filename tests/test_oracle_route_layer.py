@@ -65,6 +65,61 @@ def test_permute_invariants_and_stable_sort(orc, T, E, k):
         assert np.all(np.diff(seg // (k + 1)) > 0)
 
 
+# ---------------------------------------------------------------- router GEMM + biased top-k
+def _bf16_bits(a):
+    """fp32 array -> bf16 bit patterns (round to nearest even) and the exact values."""
+    import torch
+
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16), t.double().numpy()
+
+
+def test_router_logits_exact_on_integers_and_match_blas(orc):
+    """Small integers are exact in bf16 and their dot products exact in fp64:
+    the logits equal integer matmul; on random inputs they equal a BLAS fp64
+    matmul of the same bf16 values to rounding."""
+    rng = np.random.default_rng(3)
+    xi = rng.integers(-8, 9, size=(5, 96))
+    wi = rng.integers(-8, 9, size=(7, 96))
+    xb, _ = _bf16_bits(xi)
+    wb, _ = _bf16_bits(wi)
+    assert np.array_equal(orc.router_logits(xb, wb), (xi @ wi.T).astype(np.float64))
+    xb, xv = _bf16_bits(rng.standard_normal((9, 256)))
+    wb, wv = _bf16_bits(rng.standard_normal((12, 256)) * 0.05)
+    got = orc.router_logits(xb, wb)
+    assert got.shape == (9, 12)
+    assert np.allclose(got, xv @ wv.T, rtol=1e-12, atol=1e-12)
+
+
+def test_biased_topk(orc):
+    """A zero bias is plain top-k; a dominating bias forces its expert into
+    every token's selection while the weights stay the softmax of the chosen
+    experts' unbiased logits; brute force on fp32 scores with ties."""
+    rng = np.random.default_rng(8)
+    l = rng.standard_normal((20, 16)).astype(np.float32)
+    ids0, w0 = orc.route_topk(l, 4)
+    ids1, w1 = orc.route_topk_biased(l, np.zeros(16, np.float32), 4)
+    assert np.array_equal(ids0, ids1) and np.array_equal(w0, w1)
+    ids_n, _ = orc.route_topk_biased(l, None, 4)
+    assert np.array_equal(ids_n, ids0)
+    bias = np.zeros(16, np.float32)
+    bias[11] = 100.0
+    ids, w = orc.route_topk_biased(l, bias, 4)
+    assert np.all(ids[:, 0] == 11)
+    for t in range(20):
+        sel = l[t, ids[t]].astype(np.float64)
+        assert np.allclose(w[t], sps.softmax(sel), rtol=1e-14)
+        rest = np.setdiff1d(np.arange(16), ids[t])
+        assert np.min((l[t] + bias)[ids[t]]) >= np.max((l[t] + bias)[rest])
+    # ties in the biased score resolve to the lowest index
+    lt = rng.integers(-2, 3, size=(30, 10)).astype(np.float32)
+    bt = rng.integers(-1, 2, size=10).astype(np.float32)
+    ids, _ = orc.route_topk_biased(lt, bt, 5)
+    score = (lt + bt).astype(np.float32)
+    want = np.argsort(-score, axis=1, kind="stable")[:, :5]
+    assert np.array_equal(ids, want)
+
+
 # ---------------------------------------------------------------- expert layer
 def _random_layer(orc, rng, T, H, I, E, k, fmt, std=0.05, act_fmt=None):
     w1c, w1s, w2c, w2s = [], [], [], []
