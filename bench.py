@@ -413,7 +413,39 @@ def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us):
     oai_us = time_fused(layer, x, logits, out, args.steps, args.warmup, flush, stream, dev, oai)
     if mx.moe_get_status(layer.workspace(wl.T)):
         raise RuntimeError(f"{wl.name}: device status error in a layer variant")
-    return {"shared_expert": {"folded_us": folded_us, "dense_us": dense_us,
+    # the router GEMM with top-k in its epilogue, on this workload's T, H, E, k
+    g = torch.Generator(device=dev).manual_seed(7)
+    w_r = (torch.randn(wl.E, wl.H, generator=g, device=dev) / wl.H ** 0.5).to(torch.bfloat16)
+    ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
+    tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+    rws = mx.alloc_workspace(256, dev)
+    for _ in range(args.warmup):
+        mx.moe_route_gemm_topk(x, w_r, wl.k, rws, topk_ids=ids, topk_w=tw)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(graph, stream=cap):
+            mx.moe_route_gemm_topk(x, w_r, wl.k, rws, topk_ids=ids, topk_w=tw)
+    stream.wait_stream(cap)
+    graph.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(1)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if mx.moe_get_status(rws):
+        raise RuntimeError(f"{wl.name}: device status error in the router GEMM")
+    router_us = 1e3 * float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    router = {"us": router_us, "tflops": 2.0 * wl.T * wl.H * wl.E / (router_us * 1e-6) / 1e12,
+              "gbs": (wl.E * wl.H * 2 + wl.T * wl.H * 2 + wl.T * wl.k * 8) / (router_us * 1e-6) / 1e9,
+              "launches": 1, "timing": "CUDA graph of the call, CUDA events, L2 flushed"}
+    return {"router_gemm_topk": router,
+            "shared_expert": {"folded_us": folded_us, "dense_us": dense_us,
                               "folded_speedup": dense_us / folded_us,
                               "dense_launches": mx.moe_forward_launches_ex(wl.T, wl.H, wl.I, wl.E, wl.k, layer.fmt, dense)},
             "swiglu_oai": {"us_per_layer": oai_us, "alpha": 1.702, "limit": 7.0}}

@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmxmoe.so")
 STAMP_FILE = LIB + ".stamp"
-SOURCES = ["prep.cu", "gemm.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["prep.cu", "gemm.cu", "router.cu", "api.cu", "noalloc.cu"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

@@ -455,6 +455,35 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
                    f.perm.status, s, 2, shared);
 }
 
+int moe_route_gemm_topk(const void* x_bf16, const void* w_router_bf16, const float* bias, int T, int H, int E,
+                        int k, float* logits, int32_t* topk_ids, float* topk_w, void* ws, size_t ws_bytes,
+                        mx_stream_t stream) {
+  if (T < 0 || H <= 0 || E <= 0) return MX_ERR_INVALID_ARG;
+  const bool select = topk_ids != nullptr || topk_w != nullptr;
+  if (select && (!topk_ids || !topk_w || k < 1 || k > E)) return MX_ERR_INVALID_ARG;
+  if (!select && !logits) return MX_ERR_INVALID_ARG;
+  if (H % 64 || E > 512 || (select && k > 16)) return MX_ERR_UNSUPPORTED;
+  if (!ws) return MX_ERR_INVALID_ARG;
+  if (ws_bytes < 256) return MX_ERR_WORKSPACE;
+  if (T == 0) return MX_OK;
+  if (!x_bf16 || !w_router_bf16) return MX_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(w_router_bf16, 16) || !aligned(ws, 256)) return MX_ERR_ALIGNMENT;
+  RouterArgs a{};
+  a.x = x_bf16;
+  a.w = w_router_bf16;
+  a.bias = bias;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = select ? k : 0;
+  a.logits = logits;
+  a.ids = topk_ids;
+  a.topk_w = topk_w;
+  a.status = static_cast<int*>(ws);
+  a.wait_limit_ns = g_wait_limit_ns;
+  return cuda_status(launch_router(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int moe_forward_launches(int T, int H, int I, int E, int k, int fmt) {
   return moe_forward_launches_ex(T, H, I, E, k, fmt, nullptr);
 }

@@ -75,6 +75,20 @@ cudaError_t launch_prepare_weights(const uint8_t* codes, const uint8_t* scales,
 
 cudaError_t launch_zero(void* p, size_t bytes, cudaStream_t s);
 
+// ---- router.cu
+struct RouterArgs {
+  const void* x;         // bf16 [T, H]
+  const void* w;         // bf16 [E, H]
+  const float* bias;     // [E] or null
+  int T, H, E, k;
+  float* logits;         // [T, E] or null
+  int32_t* ids;          // [T, k] or null (logits only)
+  float* topk_w;         // [T, k]
+  int* status;
+  uint64_t wait_limit_ns;
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
 // ---- gemm.cu
 struct GemmArgs {
   int epi;               // 0: gate/up + SwiGLU + requant, 1: down + combine

@@ -53,6 +53,7 @@ SIGNATURES = {
     "mx_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
     "mx_quantize_weights": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
+    "moe_route_gemm_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_workspace_size": (_SZ, [_I, _I, _I]),
     "moe_permute": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_no_alloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P]),
@@ -154,6 +155,16 @@ def moe_route_topk(logits, k, topk_ids, topk_w, stream=None):
     T, E = logits.shape
     _check(lib().moe_route_topk(_ptr(logits), T, E, k, _ptr(topk_ids), _ptr(topk_w), _stream(stream)),
            "moe_route_topk")
+
+
+def moe_route_gemm_topk(x, w_router, k, ws, bias=None, logits=None, topk_ids=None, topk_w=None, stream=None):
+    """Router GEMM (bf16 x [T, H] . w_router [E, H]^T, fp32) with top-k in its
+    epilogue; logits, ids and weights are written where tensors are given."""
+    T, H = x.shape
+    E = w_router.shape[0]
+    _check(lib().moe_route_gemm_topk(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, _ptr(logits), _ptr(topk_ids),
+                                     _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_route_gemm_topk")
 
 
 def moe_permute_workspace_size(T, E, k) -> int:

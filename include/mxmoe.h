@@ -111,6 +111,27 @@ MX_API int mx_quantize_weights(const float* w, int64_t rows, int K, int fmt, uin
 MX_API int moe_route_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                    mx_stream_t stream);
 
+/* Router GEMM with top-k in its epilogue (the step ahead of moe_route_topk):
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h]   (bf16 inputs, fp32 accumulation
+ *     on the tensor cores; products of bf16 values are exact in fp32)
+ *   topk_ids[t, :] = the k experts with the largest score logit + bias[e]
+ *     (one fp32 addition), lowest index on ties, descending score order
+ *   topk_w[t, :] = softmax of the chosen experts' unbiased logits (fp32).
+ *   x_bf16 [T, H], w_router_bf16 [E, H] row-major, 16-byte aligned.
+ *   bias [E] fp32 or NULL (no bias): a load-balancing bias that steers which
+ *     experts are chosen but not their weights (this library's reading; the
+ *     pages give no router).  logits [T, E] or NULL.  topk_ids and topk_w
+ *     both NULL: logits only (then logits must be given).
+ *   ws: a 256-byte-aligned workspace of at least 256 bytes, zero-filled once;
+ *     its first word is the status word moe_get_status reads.
+ * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H % 64, E > 512, k > 16),
+ * MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE.
+ * Source: the MI355X page, Figure 4 and its passage (tokens are routed to
+ * experts by router scores; the router itself is not printed). */
+MX_API int moe_route_gemm_topk(const void* x_bf16, const void* w_router_bf16, const float* bias, int T, int H,
+                               int E, int k, float* logits, int32_t* topk_ids, float* topk_w, void* ws,
+                               size_t ws_bytes, mx_stream_t stream);
+
 /* Bytes of workspace moe_permute needs. */
 MX_API size_t moe_permute_workspace_size(int T, int E, int k);
 
