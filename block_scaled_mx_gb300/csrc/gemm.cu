@@ -57,7 +57,10 @@ constexpr int kEpiWarps = 8;
 // 8 columns of fp32 (down)
 __host__ __device__ constexpr uint32_t epi_buf_bytes(int epi) { return epi == 0 ? 512u : 1024u; }
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfColsPerChunk = 24;  // per K chunk: SFA sub0 (+0), SFA sub1 (+8), SFB (+16)
+// per K chunk: SFA of row block 0 (+0), of row block 1 (+8), SFB (+16); a CTA
+// pair's CTA has one row block: SFA (+0), SFB (+8)
+constexpr uint32_t kSfColsPerChunk = 24;
+constexpr uint32_t kSfColsPerChunkPair = 16;
 constexpr int kMaxStages = 8;
 constexpr int kMaxDevices = 64;
 
@@ -85,8 +88,11 @@ struct GemmParams {
   float* out;
   int* status;
   unsigned long long wait_limit_ns;
-  uint32_t off_a, off_b, off_meta, off_bar, off_epi;
+  uint32_t off_a, off_b, off_meta, off_bar, off_epi, off_x;
   uint32_t sf_col0;
+  uint32_t sfc;     // tensor-memory scale columns per K chunk: 24 (two A blocks), 16 (pair: one)
+  uint32_t acc_cols; // accumulator columns per buffer: 2 bn, or bn with a pair
+  uint32_t xs;      // pair gate/up: row stride (words) of the exchange buffer
   int gather4;      // B rows gathered by token with TMA gather4 (else one 2-D box of slot rows)
   int pdl;          // see GemmArgs::pdl
   int kps;          // 128-wide K chunks per pipeline stage (1 or 2)
@@ -109,6 +115,8 @@ struct Shared {
   uint64_t* drain;
   uint64_t* exit_bar;  // CTA pair: the peer has finished every role
   uint64_t* peer_full; // CTA pair, rank 0: rank 1's copy of the stage is full
+  uint64_t* xfull;     // CTA pair gate/up: the partner has written this CTA's exchange buffer
+  uint64_t* xfree;     // CTA pair gate/up: the partner has read its exchange buffer (free to write)
   uint32_t* tmem_slot;
   unsigned* sf_cnt;    // CTA pair: scale warps done with each pipeline slot
   uint32_t rank;       // rank in the CTA pair (0 without one)
@@ -192,18 +200,18 @@ __device__ __forceinline__ void arrive_leader(const Shared& sh, uint64_t* bar) {
 }
 
 // One 128-wide K chunk of a tile: four K = 32 steps, each an MMA per row
-// block (gate and up, or two row blocks of W2) into its own accumulator;
-// `accum` turns on after the tile's first step.
+// block (gate and up, or two row blocks of W2) into its own accumulator, or,
+// with a CTA pair, one M = 256 MMA over both CTAs' row blocks; `accum` turns
+// on after the tile's first step.
 template <bool PAIR, bool TWO>
 __device__ __forceinline__ void issue_chunk(uint32_t d0, uint32_t d1, uint32_t a_lo, uint32_t b_lo, uint32_t sf,
                                             const uint32_t (&idesc)[4], uint32_t& accum) {
 #pragma unroll
   for (int kb = 0; kb < 4; ++kb) {
     if (PAIR) {
-      mma_mxf8f6f4_pair_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
-      if (TWO)
-        mma_mxf8f6f4_pair_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
-                             sf + 16u, accum);
+      // one M = 256 MMA: each CTA's own row block, its A scales at +0, the B
+      // scales of all N columns at +8
+      mma_mxf8f6f4_pair_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 8u, accum);
     } else {
       mma_mxf8f6f4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 0u, sf + 16u, accum);
       if (TWO)
@@ -247,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
   sh.abort_flag = reinterpret_cast<volatile int*>(bars + 2 * S + 7);
   sh.peer_full = bars + 2 * S + 8;                                 // S barriers
-  sh.sf_cnt = reinterpret_cast<unsigned*>(bars + 3 * S + 8);       // S counters
+  sh.xfull = bars + 3 * S + 8;
+  sh.xfree = bars + 3 * S + 9;
+  sh.sf_cnt = reinterpret_cast<unsigned*>(bars + 3 * S + 10);      // S counters
   sh.rank = PAIR ? cluster_ctarank() : 0u;
   sh.hint_ns = p.hint_ns;
   const bool leader = sh.rank == 0;
@@ -276,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(sh.drain), 1);
     mbar_init(smem_u32(sh.exit_bar), 1);
+    mbar_init(smem_u32(sh.xfull), kEpiWarps);
+    mbar_init(smem_u32(sh.xfree), kEpiWarps);
     for (int s = 0; s < S; ++s) sh.sf_cnt[s] = 0u;
     *sh.abort_flag = 0;
     fence_mbar_init();
@@ -354,7 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool b_ready = p.pdl != 2;  // mode 2: the B rows appear when the previous grid completes
     for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
+      // the tile's first prepared row block (a pair's CTA: its own block)
+      const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
       // a pair's MMA takes token rows [0, N/2) from rank 0 and [N/2, N) from
       // rank 1, N the tile's rows rounded up to 16
       int n_mma = (tl.rows + 15) & ~15;
@@ -375,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.brows) * 128u;
-      const uint32_t bytes = (2u * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
+      const uint32_t bytes = ((PAIR ? 1u : 2u) * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
@@ -388,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, bytes);
           for (int u = 0; u < kps; ++u) {
             const int kc = ks + u;
-            uint8_t* a_s = base + p.off_a + (su + u) * 32768u;
-            // blocks 2m and 2m + 1 (a box two blocks deep; past the table's end
-            // the TMA fills zeros and still counts the whole box)
-            const int blk0 = ((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m;
+            uint8_t* a_s = base + p.off_a + (su + u) * (PAIR ? 16384u : 32768u);
+            // blocks 2m and 2m + 1 (a box two blocks deep, one with a pair; past
+            // the table's end the TMA fills zeros and still counts the whole box)
+            const int blk0 = ((tl.e + p.e_base) * NK + kc) * p.RB + blk_row;
             tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
           }
         }
@@ -473,14 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = unit0; t < total && ok; t += unit_step) {
         const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-        const int m = PAIR ? 2 * tl.m : tl.m;   // a pair's tiles both have two row blocks
-        const bool two = p.epi == 0 || (2 * m + 1 < p.RB);
+        const bool two = !PAIR && (p.epi == 0 || (2 * tl.m + 1 < p.RB));
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
         if (!wait_bar<PAIR>(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
         tc_fence_after();
-        const uint32_t d0 = tbase + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
-        const uint32_t d1 = tbase + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
+        const uint32_t d0 = tbase + ab * p.acc_cols;
+        const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn);
         uint32_t idesc[4];
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, kM, n_mma, kb, kb);
@@ -501,19 +513,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tensor memory): the single issuing thread's work between two MMAs
           // is tensor time
           const uint32_t slot0 = s * kps;
+          constexpr uint32_t a16 = (PAIR ? 16384u : 32768u) >> 4;  // A slot stride in 16-byte units
+          constexpr uint32_t sfc = PAIR ? kSfColsPerChunkPair : kSfColsPerChunk;
           if (two) {
-            issue_chunk<PAIR, true>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
-                                    sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            issue_chunk<PAIR, true>(d0, d1, a_lo0 + slot0 * a16, b_lo0 + slot0 * b_stride16, sf_base + slot0 * sfc,
+                                    idesc, accum);
             if (kps == 2)
-              issue_chunk<PAIR, true>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4), b_lo0 + (slot0 + 1) * b_stride16,
-                                      sf_base + (slot0 + 1) * kSfColsPerChunk, idesc, accum);
+              issue_chunk<PAIR, true>(d0, d1, a_lo0 + (slot0 + 1) * a16, b_lo0 + (slot0 + 1) * b_stride16,
+                                      sf_base + (slot0 + 1) * sfc, idesc, accum);
           } else {
-            issue_chunk<PAIR, false>(d0, d1, a_lo0 + slot0 * (32768u >> 4), b_lo0 + slot0 * b_stride16,
-                                     sf_base + slot0 * kSfColsPerChunk, idesc, accum);
+            issue_chunk<PAIR, false>(d0, d1, a_lo0 + slot0 * a16, b_lo0 + slot0 * b_stride16, sf_base + slot0 * sfc,
+                                     idesc, accum);
             if (kps == 2)
-              issue_chunk<PAIR, false>(d0, d1, a_lo0 + (slot0 + 1) * (32768u >> 4),
-                                       b_lo0 + (slot0 + 1) * b_stride16, sf_base + (slot0 + 1) * kSfColsPerChunk,
-                                       idesc, accum);
+              issue_chunk<PAIR, false>(d0, d1, a_lo0 + (slot0 + 1) * a16, b_lo0 + (slot0 + 1) * b_stride16,
+                                       sf_base + (slot0 + 1) * sfc, idesc, accum);
           }
           if (PAIR) mma_commit_pair(smem_u32(&sh.empty[s]), 3);
           else mma_commit(smem_u32(&sh.empty[s]));
@@ -561,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
-      const bool two = 2 * m + 1 < p.RB;
+      // the tile's first prepared row block (a pair's CTA: its own, the only one)
+      const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
+      const bool two = !PAIR && 2 * tl.m + 1 < p.RB;
       // rows 32j + lane of this tile: the word offset of their scale rows
       // (-1: a padding row)
       int roww[8];
@@ -590,14 +604,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sft = tid - kWarpSf0 * 32;
         for (int i = sft; i < NK * lines; i += 128) {
           const int kc = i / lines, line = i - kc * lines;
-          const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m) * 32;
+          const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + blk_row) * 32;
           prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
         }
       }
       auto load = [&](ScaleBuf& b, int kc) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bsc + roww[j] + kc) : 0x7F7F7F7Fu;
-        const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + 2 * m) * 32;
+        const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + blk_row) * 32;
         b.a0 = __ldg(blk + lane);
         b.a1 = two ? __ldg(blk + 32 + lane) : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       };
@@ -618,13 +632,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) return false;
         }
         // chunk slot: A scales of row block 2m at +0, of 2m + 1 at +8, B at
-        // +16 (column j of a block holds rows 32j + lane; B: j < 8, N <= 256)
-        const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + static_cast<uint32_t>(u)) * kSfColsPerChunk;
+        // +16 (column j of a block holds rows 32j + lane; B: j < 8, N <= 256);
+        // a pair's CTA: its one A block at +0, B at +8
+        constexpr uint32_t sfc = PAIR ? kSfColsPerChunkPair : kSfColsPerChunk;
+        constexpr uint32_t b_col = PAIR ? 8u : 16u;
+        const uint32_t col = col0 + (s * static_cast<uint32_t>(kps) + static_cast<uint32_t>(u)) * sfc;
         __syncwarp();
         tmem_st_32x32b_x4(col + 0u, cur.a0.x, cur.a0.y, cur.a0.z, cur.a0.w);
-        tmem_st_32x32b_x4(col + 8u, cur.a1.x, cur.a1.y, cur.a1.z, cur.a1.w);
-        if (bn > 128) tmem_st_32x32b_x8(col + 16u, cur.bw);
-        else tmem_st_32x32b_x4(col + 16u, cur.bw[0], cur.bw[1], cur.bw[2], cur.bw[3]);
+        if (!PAIR) tmem_st_32x32b_x4(col + 8u, cur.a1.x, cur.a1.y, cur.a1.z, cur.a1.w);
+        if (bn > 128) tmem_st_32x32b_x8(col + b_col, cur.bw);
+        else tmem_st_32x32b_x4(col + b_col, cur.bw[0], cur.bw[1], cur.bw[2], cur.bw[3]);
         if (u != kps - 1) return true;
         tmem_st_wait();
         tc_fence_before();
@@ -673,9 +690,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(p.epi);
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
+    uint32_t xph = 0;  // pair gate/up: phase of the exchange barriers
     for (int t = unit0; t < total; t += unit_step) {
       const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-      const int m = PAIR ? 2 * tl.m + static_cast<int>(sh.rank) : tl.m;
       ab = ab_next;
       aph = aph_next;
       if (++ab_next == acc_bufs) {
@@ -686,10 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       __syncwarp();
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-      const uint32_t d0 = tbase + lane_base + (ab * 2u + 0u) * static_cast<uint32_t>(p.bn);
-      const uint32_t d1 = tbase + lane_base + (ab * 2u + 1u) * static_cast<uint32_t>(p.bn);
+      const uint32_t d0 = tbase + lane_base + ab * p.acc_cols;
+      const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn);
       if (p.epi == 0) {
-        const int i0 = m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
+        const int i0 = tl.m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
         const int I = p.I, I32 = p.I / 32;
         uint8_t* const h_codes = p.h_codes;
         uint8_t* const h_scales = p.h_scales;
@@ -747,6 +764,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             h_scales[static_cast<size_t>(tl.p0 + c0 + lane) * I32 + i0 / 32] = static_cast<uint8_t>(my_s + 127);
           __syncwarp();
         };
+        if (PAIR) {
+          // rank 0 holds g (gate block m), rank 1 u (up block m), for all N
+          // tokens of the tile; rank 0 finishes tokens [0, N/2), rank 1
+          // [N/2, N), each after receiving the other's values for its half in
+          // its exchange buffer (rows of I x its tokens, row stride xs words)
+          int nmma = (tl.rows + 15) & ~15;
+          if (nmma < 16) nmma = 16;
+          const int hw = nmma >> 1;
+          const int own0 = static_cast<int>(sh.rank) * hw, oth0 = hw - own0;
+          const uint32_t xs = p.xs;
+          float* const xmine = reinterpret_cast<float*>(base + p.off_x);
+          const uint32_t xpeer = mapa_shared(smem_u32(xmine), sh.rank ^ 1u);
+          const uint32_t row = static_cast<uint32_t>(32 * q + lane);
+          // the partner has read its buffer for the previous tile
+          if (!warp_wait_bar<PAIR>(sh, sh.xfree, xph ^ 1u, p.wait_limit_ns, p.status)) break;
+          for (int c0 = oth0 + 8 * half; c0 < oth0 + hw && c0 < tl.rows; c0 += 16) {
+            uint32_t v[8];
+            __syncwarp();
+            tmem_ld_32x32b_x8(d0 + c0, v);
+            tmem_ld_wait();
+            const uint32_t a = xpeer + (row * xs + static_cast<uint32_t>(c0 - oth0)) * 4u;
+            st_shared_cluster_v4(a, v[0], v[1], v[2], v[3]);
+            st_shared_cluster_v4(a + 16u, v[4], v[5], v[6], v[7]);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(sh.xfull), sh.rank ^ 1u));
+          // the partner's values for this CTA's tokens have arrived
+          if (!warp_wait_bar<PAIR>(sh, sh.xfull, xph, p.wait_limit_ns, p.status)) break;
+          for (int c0 = own0 + 8 * half; c0 < own0 + hw && c0 < tl.rows; c0 += 16) {
+            uint32_t mine[8], other[8];
+            __syncwarp();
+            tmem_ld_32x32b_x8(d0 + c0, mine);
+            const uint4* xp = reinterpret_cast<const uint4*>(xmine + row * xs + static_cast<uint32_t>(c0 - own0));
+            const uint4 o0 = xp[0], o1 = xp[1];
+            other[0] = o0.x, other[1] = o0.y, other[2] = o0.z, other[3] = o0.w;
+            other[4] = o1.x, other[5] = o1.y, other[6] = o1.z, other[7] = o1.w;
+            tmem_ld_wait();
+            if (sh.rank == 0) process(mine, other, c0);
+            else process(other, mine, c0);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(sh.xfree), sh.rank ^ 1u));
+          xph ^= 1u;
+        } else {
         uint32_t ga[8], ua[8], gb[8], ub[8];
         int c0 = 8 * half;
         if (c0 < tl.rows) {
@@ -774,8 +835,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
           c0 = c2;
         }
+        }
       } else {
-        const bool two = 2 * m + 1 < p.RB;
+        // W2 row blocks 2m and 2m + 1 (a pair's CTA: its own one)
+        const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
+        const bool two = !PAIR && 2 * tl.m + 1 < p.RB;
         float* const out = p.out;
         const int H = p.H;
         float* const ebf = reinterpret_cast<float*>(ebuf);
@@ -802,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int hh = 0; hh < 2; ++hh)
               if (c0 + 16 * hh < tl.rows) tmem_ld_32x32b_x16(d + c0 + 16 * hh, a[hh]);
             tmem_ld_wait();
-            const int o0 = m * 256 + sub * 128 + 32 * q;  // this warp's 32 rows of H
+            const int o0 = (blk_row + sub) * 128 + 32 * q;  // this warp's 32 rows of H
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const int h0 = 16 * hh;
@@ -896,10 +960,10 @@ static int sm_count_gemm() {
 static uint32_t weight_block_tx_bytes(int fmt) { return fmt == MX_E4M3 ? 16384u : 8192u; }
 
 bool pair_supported(const GemmArgs& a) {
-  // both CTAs of a pair take full two-block weight tiles, with token rows in
-  // slot order (2-D boxes)
+  // each CTA of a pair takes one row block of every weight tile (so every
+  // tile needs both), with token rows in slot order (2-D boxes) split in halves
   const int rows = a.epi == 0 ? 2 * a.I : a.H;
-  return !a.gather4 && (rows / 128) % 4 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
+  return !a.gather4 && (rows / 128) % 2 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -924,8 +988,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.K = a.epi == 0 ? a.H : a.I;
   p.NK = p.K / 128;
   p.RB = rows / 128;
+  // weight tiles of two row blocks (gate and up block m, or W2 blocks 2m and
+  // 2m + 1); a CTA pair splits each tile's two blocks between its CTAs
   p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
-  if (pair) p.NM /= 2;   // pair tiles: two weight tiles each
   // down GEMM: split the weight tiles into groups so that one group's slice of
   // `out` (T rows x the group's 256-column blocks, fp32) stays within ~16 MB of
   // L2 while every expert's atomic combine lands on it
@@ -942,6 +1007,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   p.bn = a.bn;
   p.brows = pair ? a.bn / 2 : a.bn;
+  p.sfc = pair ? kSfColsPerChunkPair : kSfColsPerChunk;
+  p.acc_cols = (pair ? 1u : 2u) * static_cast<uint32_t>(a.bn);
+  p.xs = static_cast<uint32_t>(a.bn / 2 + 4);
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
   const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt, a.epi == 0 ? 1 : 0);
@@ -968,15 +1036,19 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   int max_smem = 0;
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   const uint32_t epi_bytes = kEpiWarps * epi_buf_bytes(a.epi);
-  const uint32_t fixed = 1024u /*align slack*/ + meta_bytes + 512u /*barriers*/ + 128u /*static*/ + epi_bytes;
+  // a pair's gate/up epilogue receives the partner's half of the tokens here
+  const uint32_t x_bytes = (pair && a.epi == 0) ? 128u * p.xs * 4u : 0u;
+  const uint32_t fixed =
+      1024u /*align slack*/ + meta_bytes + 512u /*barriers*/ + 128u /*static*/ + epi_bytes + x_bytes;
+  const uint32_t a_stage = (pair ? 16384u : 32768u);  // unpacked weight blocks per K chunk
   const char* env_stages = std::getenv("MXMOE_STAGES");  // tuning override (only lowers)
   auto plan = [&](int kps, int* acc_bufs, uint32_t* sf_col0) {
     // two accumulator buffers (the epilogue of one tile overlaps the next
     // tile's MMAs) whenever they leave tensor memory for two stages of scales
-    *acc_bufs = (4u * static_cast<uint32_t>(p.bn) + 2u * kSfColsPerChunk * kps <= kTmemCols) ? 2 : 1;
-    *sf_col0 = 2u * static_cast<uint32_t>(*acc_bufs) * static_cast<uint32_t>(p.bn);
-    if (*sf_col0 + 2u * kSfColsPerChunk * kps > kTmemCols) return 0;
-    const uint32_t per_stage = (32768u + static_cast<uint32_t>(p.brows) * 128u) * static_cast<uint32_t>(kps);
+    *acc_bufs = (2u * p.acc_cols + 2u * p.sfc * kps <= kTmemCols) ? 2 : 1;
+    *sf_col0 = static_cast<uint32_t>(*acc_bufs) * p.acc_cols;
+    if (*sf_col0 + 2u * p.sfc * kps > kTmemCols) return 0;
+    const uint32_t per_stage = (a_stage + static_cast<uint32_t>(p.brows) * 128u) * static_cast<uint32_t>(kps);
     if (static_cast<uint32_t>(max_smem) <= fixed) return 0;
     int st = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
     if (st > kMaxStages) st = kMaxStages;
@@ -984,7 +1056,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
       const int v = std::atoi(env_stages);
       if (v >= 2 && v < st) st = v;
     }
-    const int tmem_room = static_cast<int>((kTmemCols - *sf_col0) / (kSfColsPerChunk * kps));
+    const int tmem_room = static_cast<int>((kTmemCols - *sf_col0) / (p.sfc * kps));
     if (st > tmem_room) st = tmem_room;
     return st >= 2 ? st : 0;
   };
@@ -1006,7 +1078,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.stages = stages;
   uint32_t off = 0;
   p.off_a = off;
-  off += static_cast<uint32_t>(stages * p.kps) * 32768u;
+  off += static_cast<uint32_t>(stages * p.kps) * a_stage;
   p.off_b = off;
   off += static_cast<uint32_t>(stages * p.kps) * p.brows * 128u;
   p.off_meta = off;
@@ -1015,6 +1087,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   off += 512u;
   p.off_epi = off;
   off += epi_bytes;
+  p.off_x = off;
+  off += x_bytes;
   const size_t smem = static_cast<size_t>(off) + 1024u;
 
   // tensor maps
@@ -1023,7 +1097,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   {
     cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(nblk)};
     cuuint64_t strides[2];
-    cuuint32_t box[3] = {128, 128, 2};  // two row blocks per box
+    cuuint32_t box[3] = {128, 128, pair ? 1u : 2u};  // the tile's two row blocks (one per CTA of a pair)
     cuuint32_t es[3] = {1, 1, 1};
     CUtensorMapDataType dt;
     if (a.fmt == MX_E4M3) {
