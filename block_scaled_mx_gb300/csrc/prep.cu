@@ -240,9 +240,20 @@ PermuteScratch permute_scratch_carve(void* ws, int T, int E, int k) {
   return sc;
 }
 
+// Dynamic shared memory of one permutation block: per warp and expert the
+// lane masks and their exclusive prefix over warps, E + 2 ints of scan space,
+// and the ids of the block's tokens.
+static size_t permute_block_smem(int T, int E, int k) {
+  const int nt = T < kPermuteChunk ? T : kPermuteChunk;
+  return (static_cast<size_t>(2 * (kPermuteChunk / 32)) * E + (E + 2) + static_cast<size_t>(nt) * k) * 4;
+}
+
 // One chunk of pass 1 (and, for a single chunk, the whole permutation), run by
-// one block of kPermuteChunk threads.  `bits` is the dynamic shared scratch:
-// [8 warps][E] lane masks followed by E + 2 ints of scan space.
+// one block of kPermuteChunk threads.  The loops over a token's k slots stay
+// rolled and read the ids from shared memory: this code runs once per call, in
+// one block, right after other kernels have streamed far more than L2 holds,
+// so its instructions come from DRAM and its length, not its arithmetic, sets
+// its latency.
 __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ ids, int T, int E,
                                                     int k, int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets,
@@ -253,62 +264,76 @@ __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ 
   __shared__ int s_is_last;
   __shared__ int s_warp_tot[kWarps];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint32_t* const pre = bits + kWarps * E;                   // [warp][E]: lanes of earlier warps
+  int* const scan = reinterpret_cast<int*>(pre + kWarps * E);  // E + 2
+  int* const s_ids = scan + E + 2;                            // [token of the chunk][k]
+  const int t0 = chunk * kPermuteChunk;
+  const int nt = min(kPermuteChunk, T - t0);
+  const int n_ids = nt * k;
+  // the chunk's ids into shared memory, eight coalesced loads in flight per thread
+  const int32_t* const src = ids + static_cast<int64_t>(t0) * k;
+  for (int i0 = 0; i0 < n_ids; i0 += 8 * kPermuteChunk) {
+    int v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kPermuteChunk + tid;
+      v[u] = i < n_ids ? __ldcg(src + i) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * kPermuteChunk + tid;
+      if (i < n_ids) s_ids[i] = v[u];
+    }
+  }
   for (int i = tid; i < kWarps * E; i += blockDim.x) bits[i] = 0u;
   __syncthreads();
-  const int t = chunk * kPermuteChunk + tid;
-  const bool valid = t < T;
-  int my_e[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    my_e[j] = -1;
-    if (j < k && valid) {
-      int e = __ldcg(&ids[static_cast<int64_t>(t) * k + j]);
+  const int t = t0 + tid;
+  const bool valid = tid < nt;
+  int* const my_ids = s_ids + tid * k;
+  // per warp and expert, the lanes (tokens) routed to it; an id out of range
+  // is reported and its slot dropped
+  if (valid) {
+    for (int j = 0; j < k; ++j) {
+      const int e = my_ids[j];
       if (e < 0 || e >= E) {
         set_status(sc.status, MX_ERR_DEVICE_ARG);
-        e = -1;
+        my_ids[j] = -1;
+      } else {
+        atomicOr(&bits[warp * E + e], 1u << lane);
       }
-      my_e[j] = e;
-      if (e >= 0) atomicOr(&bits[warp * E + e], 1u << lane);
     }
   }
   __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-  int my_r[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    my_r[j] = 0;
-    if (j < k && my_e[j] >= 0) {
-      const int e = my_e[j];
-      int r = __popc(bits[warp * E + e] & lt);
-      for (int w = 0; w < warp; ++w) r += __popc(bits[w * E + e]);
-      my_r[j] = r;
-    }
-  }
+  // per expert: the chunk's count and each warp's offset inside it
   for (int e = tid; e < E; e += blockDim.x) {
     int c = 0;
-    for (int w = 0; w < kWarps; ++w) c += __popc(bits[w * E + e]);
-    sc.chunk_counts[static_cast<int64_t>(chunk) * E + e] = c;
+    for (int w = 0; w < kWarps; ++w) {
+      pre[w * E + e] = c;
+      c += __popc(bits[w * E + e]);
+    }
+    scan[e] = c;
+    if (nchunks > 1) sc.chunk_counts[static_cast<int64_t>(chunk) * E + e] = c;
   }
+  __syncthreads();
+  // a slot's rank among the chunk's slots of its expert: earlier warps, then lower lanes
+  const uint32_t lt = (1u << lane) - 1u;
   if (nchunks > 1) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < k && valid) sc.local_rank[static_cast<int64_t>(t) * k + j] = my_r[j];
+    if (valid)
+      for (int j = 0; j < k; ++j) {
+        const int e = my_ids[j];
+        if (e >= 0)
+          sc.local_rank[static_cast<int64_t>(t) * k + j] =
+              static_cast<int>(pre[warp * E + e]) + __popc(bits[warp * E + e] & lt);
+      }
     __threadfence();
     __syncthreads();
     if (tid == 0) s_is_last = (atomicAdd(sc.done, 1u) == static_cast<unsigned>(nchunks - 1));
     __syncthreads();
     if (!s_is_last) return;
     __threadfence();
-  } else {
-    __syncthreads();
-  }
-  // ---- last (or only) block: totals, exclusive scan over E+1 experts, chunk bases
-  int* scan = reinterpret_cast<int*>(bits + kWarps * E);  // E+2 ints
-  for (int e = tid; e <= E; e += blockDim.x) {
-    int c = 0;
-    if (e < E) {
-      // eight independent loads in flight at a time (the chunk counts sit in L2)
-      int ch = 0;
+    // the last block: per-expert totals over all chunks (eight loads in flight)
+    for (int e = tid; e < E; e += blockDim.x) {
+      int c = 0, ch = 0;
       for (; ch + 8 <= nchunks; ch += 8) {
         int v[8];
 #pragma unroll
@@ -317,13 +342,12 @@ __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ 
         for (int u = 0; u < 8; ++u) c += v[u];
       }
       for (; ch < nchunks; ++ch) c += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
-    } else {
-      c = T;
+      scan[e] = c;
     }
-    scan[e] = c;
-    counts[e] = c;
   }
+  if (tid == 0) scan[E] = T;  // the shared expert: every token once
   __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) counts[e] = scan[e];
   // block-wide exclusive scan of scan[0..E] (E+1 <= 1025 values): each thread
   // owns a contiguous run, warp shuffles scan the run totals.
   const int n = E + 1;
@@ -370,13 +394,15 @@ __device__ __forceinline__ void permute_count_block(const int32_t* __restrict__ 
         base += __ldcg(&sc.chunk_counts[static_cast<int64_t>(ch) * E + e]);
       }
     }
-  } else {
+  } else if (valid) {
     // single chunk: scatter directly (this block holds every token)
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < k && valid && my_e[j] >= 0)
-        sorted_slot[scan[my_e[j]] + my_r[j]] = t * (k + 1) + j;
-    if (valid) sorted_slot[scan[E] + t] = t * (k + 1) + k;
+    for (int j = 0; j < k; ++j) {
+      const int e = my_ids[j];
+      if (e >= 0)
+        sorted_slot[scan[e] + static_cast<int>(pre[warp * E + e]) + __popc(bits[warp * E + e] & lt)] =
+            t * (k + 1) + j;
+    }
+    sorted_slot[scan[E] + t] = t * (k + 1) + k;
   }
 }
 
@@ -409,7 +435,7 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
                            int32_t* offsets, int32_t* sorted_slot, const PermuteScratch& sc,
                            cudaStream_t s) {
   const int nchunks = T == 0 ? 1 : (T + kPermuteChunk - 1) / kPermuteChunk;
-  const size_t smem = static_cast<size_t>(kPermuteChunk / 32) * E * 4 + static_cast<size_t>(E + 2) * 4;
+  const size_t smem = permute_block_smem(T, E, k);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_permute_count, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -468,26 +494,20 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
   const int64_t cap = static_cast<int64_t>(sm_count()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  const size_t smem = a.permute ? static_cast<size_t>(kPermuteChunk / 32) * a.E * 4 + static_cast<size_t>(a.E + 2) * 4 : 0;
+  const size_t smem = a.permute ? permute_block_smem(a.T, a.E, a.k) : 0;
   const unsigned g = static_cast<unsigned>(blocks);
-  if (a.permute) {
-    if (a.E <= 32) k_prologue<1, true><<<g, kPermuteChunk, smem, s>>>(a);
-    else if (a.E <= 128) k_prologue<4, true><<<g, kPermuteChunk, smem, s>>>(a);
-    else if (a.E <= 512) k_prologue<16, true><<<g, kPermuteChunk, smem, s>>>(a);
-    else {
-      if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k_prologue<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-      }
-      k_prologue<32, true><<<g, kPermuteChunk, smem, s>>>(a);
-    }
-  } else {
-    if (a.E <= 32) k_prologue<1, false><<<g, kPermuteChunk, 0, s>>>(a);
-    else if (a.E <= 128) k_prologue<4, false><<<g, kPermuteChunk, 0, s>>>(a);
-    else if (a.E <= 512) k_prologue<16, false><<<g, kPermuteChunk, 0, s>>>(a);
-    else k_prologue<32, false><<<g, kPermuteChunk, 0, s>>>(a);
+  void (*kern)(PrologueArgs);
+  if (a.permute)
+    kern = a.E <= 32 ? k_prologue<1, true> : a.E <= 128 ? k_prologue<4, true>
+         : a.E <= 512 ? k_prologue<16, true> : k_prologue<32, true>;
+  else
+    kern = a.E <= 32 ? k_prologue<1, false> : a.E <= 128 ? k_prologue<4, false>
+         : a.E <= 512 ? k_prologue<16, false> : k_prologue<32, false>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
   }
+  kern<<<g, kPermuteChunk, smem, s>>>(a);
   return cudaGetLastError();
 }
 
