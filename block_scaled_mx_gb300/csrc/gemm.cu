@@ -399,14 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t su = s * static_cast<uint32_t>(kps);  // first chunk slot
         if (lane == 0) {
           mbar_arrive_expect_tx(full, bytes);
-          for (int u = 0; u < kps; ++u) {
-            const int kc = ks + u;
-            uint8_t* a_s = base + p.off_a + (su + u) * (PAIR ? 16384u : 32768u);
-            // blocks 2m and 2m + 1 (a box two blocks deep, one with a pair; past
-            // the table's end the TMA fills zeros and still counts the whole box)
-            const int blk0 = ((tl.e + p.e_base) * NK + kc) * p.RB + blk_row;
-            tma_load_3d(smem_u32(a_s), &tm_a, 0, 0, blk0, full);
-          }
+          // the stage's weight blocks in one copy: row blocks 2m and 2m + 1 (one
+          // with a pair; a block past the last row block is filled with zeros and
+          // still counted) of its kps K chunks, chunk-major in shared memory.
+          // Fewer, larger copies: a TMA copy has a fixed cost of its own, and a
+          // stage of MXFP4 blocks is only 8 KB per block.
+          uint8_t* a_s = base + p.off_a + su * (PAIR ? 16384u : 32768u);
+          tma_load_4d(smem_u32(a_s), &tm_a, 0, 0, blk_row, (tl.e + p.e_base) * NK + ks, full);
         }
         if (!b_ready) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1093,23 +1092,27 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
 
   // tensor maps
   CUtensorMap tm_a, tm_b;
-  const size_t nblk = static_cast<size_t>(a.E + 1) * p.RB * p.NK;
   {
-    cuuint64_t dims[3] = {128, 128, static_cast<cuuint64_t>(nblk)};
-    cuuint64_t strides[2];
-    cuuint32_t box[3] = {128, 128, pair ? 1u : 2u};  // the tile's two row blocks (one per CTA of a pair)
-    cuuint32_t es[3] = {1, 1, 1};
+    // prepared blocks as [expert * NK + K chunk][row block][128 rows][128 K]:
+    // one box is a stage's row blocks (the tile's two, one per CTA of a pair)
+    // of kps consecutive K chunks
+    const size_t nchunk = static_cast<size_t>(a.E + 1) * p.NK;
+    cuuint64_t dims[4] = {128, 128, static_cast<cuuint64_t>(p.RB), static_cast<cuuint64_t>(nchunk)};
+    cuuint64_t strides[3];
+    cuuint32_t box[4] = {128, 128, pair ? 1u : 2u, static_cast<cuuint32_t>(p.kps)};
+    cuuint32_t es[4] = {1, 1, 1, 1};
     CUtensorMapDataType dt;
+    const cuuint64_t blk_bytes = a.fmt == MX_E4M3 ? 16384 : 8192;
     if (a.fmt == MX_E4M3) {
       dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
       strides[0] = 128;
-      strides[1] = 16384;
     } else {
       dt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
       strides[0] = 64;
-      strides[1] = 8192;
     }
-    CUresult r = encode(&tm_a, dt, 3, const_cast<void*>(a.w_prep), dims, strides, box, es,
+    strides[1] = blk_bytes;
+    strides[2] = blk_bytes * static_cast<cuuint64_t>(p.RB);
+    CUresult r = encode(&tm_a, dt, 4, const_cast<void*>(a.w_prep), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
