@@ -401,9 +401,10 @@ def time_fused(layer, x, logits, out, steps, warmup, flush, stream, dev, opts=No
     return 1e3 * float(np.mean([a.elapsed_time(b) for a, b in ev]))
 
 
-def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us):
+def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us, touched):
     """The layer variants timed beside the default: the shared expert as its own
-    dense launches (the A/B of the folded table), and the SwiGLU-OAI epilogue."""
+    dense launches (the A/B of the folded table), the SwiGLU-OAI epilogue, the
+    router GEMM, and (MXFP4 weights) MXFP4 activations on the packed-FP4 MMA."""
     from block_scaled_mx_gb300 import mxmoe as mx
 
     out = torch.empty(wl.T, wl.H, dtype=torch.float32, device=dev)
@@ -444,7 +445,20 @@ def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us):
     router = {"us": router_us, "tflops": 2.0 * wl.T * wl.H * wl.E / (router_us * 1e-6) / 1e12,
               "gbs": (wl.E * wl.H * 2 + wl.T * wl.H * 2 + wl.T * wl.k * 8) / (router_us * 1e-6) / 1e9,
               "launches": 1, "timing": "CUDA graph of the call, CUDA events, L2 flushed"}
-    return {"router_gemm_topk": router,
+    res = {}
+    if wl.fmt == "e2m1":
+        # MXFP4 activations and h: both grouped GEMMs on the packed-FP4 MMA
+        # (changes the numerics: its own oracle path and tolerance in the tests)
+        a4 = mx.layer_opts(act_fmt="e2m1")
+        a4_us = time_fused(layer, x, logits, out, args.steps, args.warmup, flush, stream, dev, a4)
+        if mx.moe_get_status(layer.workspace(wl.T)):
+            raise RuntimeError(f"{wl.name}: device status error in the MXFP4-activation layer")
+        w1b, w2b = weight_bytes_per_expert(wl)
+        res["mxfp4_activations"] = {
+            "us_per_layer": a4_us, "speedup_vs_mxfp8_activations": folded_us / a4_us,
+            "layer_roofline_frac": touched * (w1b + w2b) / (a4_us * 1e-6) / 1e9 / peaks()["hbm_gbs"],
+            "mma": "tcgen05 kind::mxf4 block_scale scale_vec::2X"}
+    return {**res, "router_gemm_topk": router,
             "shared_expert": {"folded_us": folded_us, "dense_us": dense_us,
                               "folded_speedup": dense_us / folded_us,
                               "dense_launches": mx.moe_forward_launches_ex(wl.T, wl.H, wl.I, wl.E, wl.k, layer.fmt, dense)},
@@ -580,7 +594,7 @@ def measure_workload(args, wl, dev, world, clk, with_cpu):
     e2e = max_over_ranks(float(np.mean(e2e_ms)), world, dev)
     if mx.moe_get_status(layer.workspace(T)):
         raise RuntimeError(f"{wl.name}: device status error in moe_forward")
-    variants = measure_variants(args, layer, wl, x, logits, flush, stream, dev, ms * 1e3)
+    variants = measure_variants(args, layer, wl, x, logits, flush, stream, dev, ms * 1e3, touched)
 
     pk = peaks()
     gemm1_ms = float(per[:, 3].mean())

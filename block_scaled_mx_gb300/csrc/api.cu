@@ -148,9 +148,14 @@ int read_opts(const mx_layer_opts* o, LayerOpts* out) {
     r.shared = o->shared_expert;
     r.act_fmt = o->act_fmt;
   }
-  if (r.act_fmt != MX_E4M3) return MX_ERR_UNSUPPORTED;
   *out = r;
   return MX_OK;
+}
+
+// MXFP4 activations run on kind::mxf4, which needs both operands E2M1: they
+// come with MXFP4 weights only.
+int check_act_fmt(const LayerOpts& lo, int fmt) {
+  return (lo.act_fmt == MX_E2M1 && fmt != MX_E2M1) ? MX_ERR_UNSUPPORTED : MX_OK;
 }
 
 // The experts one grouped-GEMM launch covers: n table experts from e_base
@@ -170,13 +175,15 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.bn = choose_bn(T, E, k, 0);
   a.gather4 = a.bn <= 64 ? 1 : 0;
   a.pdl = a.gather4 ? pdl : 0;
+  a.a4 = lo.act_fmt == MX_E2M1 ? 1 : 0;
   a.act = lo.act;
   a.alpha = lo.alpha;
   a.limit = lo.limit;
   a.n_exp = win.n;
   a.e_base = win.e_base;
   if (!a.gather4 && gather_rows) {
-    if (launch_gather_rows(act_codes, T, H, sorted_slot, k, n_rows, act_sorted, status, s) != cudaSuccess)
+    if (launch_gather_rows(act_codes, T, a.a4 ? H / 2 : H, sorted_slot, k, n_rows, act_sorted, status, s) !=
+        cudaSuccess)
       return MX_ERR_CUDA;
   }
   a.epi = 0;
@@ -203,7 +210,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
 int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* offsets,
               const int32_t* sorted_slot, const float* topk_w, const void* w2_prep, int fmt, int T,
               int H, int I, int E, int k, float* out, int* status, cudaStream_t s, int pdl = 0,
-              Window win = Window()) {
+              Window win = Window(), int a4 = 0) {
   const int n_rows = T * (k + 1);
   if (n_rows == 0) return MX_OK;
   GemmArgs a{};
@@ -226,6 +233,7 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.out = out;
   a.status = status;
   a.pdl = pdl;
+  a.a4 = a4;
   a.bn = choose_bn(T, E, k, 1);
   a.wait_limit_ns = g_wait_limit_ns;
   choose_pair(a);
@@ -259,6 +267,17 @@ int mx_quantize_act(const void* x_bf16, int T, int H, uint8_t* codes, uint8_t* s
   if (!aligned(x_bf16, 16) || !aligned(codes, 16)) return MX_ERR_ALIGNMENT;
   return cuda_status(launch_quantize_act(x_bf16, static_cast<int64_t>(T) * H, codes, scales,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mx_quantize_act_ex(const void* x_bf16, int T, int H, int fmt, uint8_t* codes, uint8_t* scales,
+                       mx_stream_t stream) {
+  if (T < 0 || H <= 0 || (fmt != MX_E4M3 && fmt != MX_E2M1)) return MX_ERR_INVALID_ARG;
+  if (T == 0) return MX_OK;
+  if (!x_bf16 || !codes || !scales) return MX_ERR_INVALID_ARG;
+  if (H % 32) return MX_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16)) return MX_ERR_ALIGNMENT;
+  return cuda_status(launch_quantize_act(x_bf16, static_cast<int64_t>(T) * H, codes, scales,
+                                         reinterpret_cast<cudaStream_t>(stream), fmt));
 }
 
 int mx_quantize_weights(const float* w, int64_t rows, int K, int fmt, uint8_t* codes,
@@ -344,6 +363,8 @@ int moe_grouped_gemm_swiglu_ex(const uint8_t* act_codes, const uint8_t* act_scal
   if (lo.shared != MX_SHARED_FOLDED) return MX_ERR_INVALID_ARG;
   st = check_gemm_shape(T, H, I, E, k, fmt);
   if (st != MX_OK) return st;
+  st = check_act_fmt(lo, fmt);
+  if (st != MX_OK) return st;
   if (!offsets || !w1_prep || !ws) return MX_ERR_INVALID_ARG;
   if (T == 0) return MX_OK;
   if (!act_codes || !act_scales || !sorted_slot || !h_codes || !h_scales) return MX_ERR_INVALID_ARG;
@@ -361,7 +382,22 @@ int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scale
                                   const float* topk_w, const void* w2_prep, int fmt, int T, int H,
                                   int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                                   mx_stream_t stream) {
-  int st = check_gemm_shape(T, H, I, E, k, fmt);
+  return moe_grouped_gemm_down_combine_ex(h_codes, h_scales, offsets, sorted_slot, topk_w, w2_prep, fmt, T, H, I,
+                                          E, k, out, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_grouped_gemm_down_combine_ex(const uint8_t* h_codes, const uint8_t* h_scales,
+                                     const int32_t* offsets, const int32_t* sorted_slot,
+                                     const float* topk_w, const void* w2_prep, int fmt, int T, int H,
+                                     int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                                     const mx_layer_opts* opts, mx_stream_t stream) {
+  LayerOpts lo;
+  int st = read_opts(opts, &lo);
+  if (st != MX_OK) return st;
+  if (lo.shared != MX_SHARED_FOLDED) return MX_ERR_INVALID_ARG;
+  st = check_gemm_shape(T, H, I, E, k, fmt);
+  if (st != MX_OK) return st;
+  st = check_act_fmt(lo, fmt);
   if (st != MX_OK) return st;
   if (!offsets || !w2_prep || !ws) return MX_ERR_INVALID_ARG;
   if (T == 0) return MX_OK;
@@ -371,7 +407,8 @@ int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* h_scale
     return MX_ERR_ALIGNMENT;
   if (ws_bytes < moe_gemm_workspace_size(T, H, I, E, k)) return MX_ERR_WORKSPACE;
   return run_gemm2(h_codes, h_scales, offsets, sorted_slot, topk_w, w2_prep, fmt, T, H, I, E, k, out,
-                   reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+                   reinterpret_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream), 0, Window(),
+                   lo.act_fmt == MX_E2M1 ? 1 : 0);
 }
 
 size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt) {
@@ -393,6 +430,8 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
   if (st != MX_OK) return st;
   st = check_gemm_shape(T, H, I, E, k, fmt);
   if (st != MX_OK) return st;
+  st = check_act_fmt(lo, fmt);
+  if (st != MX_OK) return st;
   if (T == 0) return MX_OK;
   if (!x_bf16 || !logits || !w1_prep || !w2_prep || !out || !ws) return MX_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(out, 16) || !aligned(w1_prep, 256) || !aligned(w2_prep, 256) ||
@@ -410,6 +449,7 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
   pa.x = static_cast<const uint4*>(x_bf16);
   pa.n8 = static_cast<int64_t>(T) * H / 8;
   pa.codes = reinterpret_cast<uint2*>(f.act_codes);
+  pa.act_e2m1 = lo.act_fmt == MX_E2M1 ? 1 : 0;
   pa.scales = f.act_scales;
   pa.logits = logits;
   pa.T = T;
@@ -432,7 +472,7 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
                    f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0, lo);
     if (st != MX_OK) return st;
     return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
-                     k, out, f.perm.status, s, 2);
+                     k, out, f.perm.status, s, 2, Window(), lo.act_fmt == MX_E2M1 ? 1 : 0);
   }
   // the shared expert as its own dense MLP: the routed experts' gate/up
   // launch, the shared expert's gate/up launch over all T tokens, then the two
@@ -449,10 +489,10 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
                  f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 2 : 0, lo, shared, false);
   if (st != MX_OK) return st;
   st = run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E, k, out,
-                 f.perm.status, s, 2, routed);
+                 f.perm.status, s, 2, routed, lo.act_fmt == MX_E2M1 ? 1 : 0);
   if (st != MX_OK) return st;
   return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E, k, out,
-                   f.perm.status, s, 2, shared);
+                   f.perm.status, s, 2, shared, lo.act_fmt == MX_E2M1 ? 1 : 0);
 }
 
 int moe_route_gemm_topk(const void* x_bf16, const void* w_router_bf16, const float* bias, int T, int H, int E,

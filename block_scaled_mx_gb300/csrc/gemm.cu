@@ -97,6 +97,9 @@ struct GemmParams {
   int pdl;          // see GemmArgs::pdl
   int kps;          // 128-wide K chunks per pipeline stage (1 or 2)
   uint32_t hint_ns; // pair: suspend-time hint of whole-warp barrier waits (0: spin)
+  int a4;           // both operands packed E2M1 (kind::mxf4): MXFP4 activations and h
+  uint32_t a_slot;  // shared-memory bytes of one K chunk of weight blocks
+  uint32_t b_row;   // shared-memory bytes of one token row of one K chunk (128, or 64 packed E2M1)
 };
 
 struct Tile {
@@ -218,6 +221,22 @@ __device__ __forceinline__ void issue_chunk(uint32_t d0, uint32_t d1, uint32_t a
         mma_mxf8f6f4_lo(d1, a_lo + (16384u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw128, idesc[kb], sf + 8u,
                         sf + 16u, accum);
     }
+    accum = 1u;
+  }
+}
+
+// The same K chunk (128 elements) with both operands packed E2M1: two K = 64
+// steps per row block, each reading two scale bytes of the rows' TMEM words
+// (sf_id 0, then 2); row block 2m + 1 starts 8 KB after block 2m.
+template <bool TWO>
+__device__ __forceinline__ void issue_chunk_a4(uint32_t d0, uint32_t d1, uint32_t a_lo, uint32_t b_lo, uint32_t sf,
+                                               const uint32_t (&idesc)[2], uint32_t& accum) {
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb) {
+    mma_mxf4_lo(d0, a_lo + 2u * kb, b_lo + 2u * kb, kDescHiSw64, idesc[kb], sf + 0u, sf + 16u, accum);
+    if (TWO)
+      mma_mxf4_lo(d1, a_lo + (8192u >> 4) + 2u * kb, b_lo + 2u * kb, kDescHiSw64, idesc[kb], sf + 8u, sf + 16u,
+                  accum);
     accum = 1u;
   }
 }
@@ -387,7 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok[j] = (tt < 0 || tt >= p.T) ? 0 : tt;
         }
       }
-      const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 512u : static_cast<uint32_t>(p.brows) * 128u;
+      const uint32_t b_row = p.b_row;
+      const int kx = p.a4 ? 64 : 128;  // bytes of a K chunk in a token row
+      const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 4u * b_row : static_cast<uint32_t>(p.brows) * b_row;
       const uint32_t bytes = ((PAIR ? 1u : 2u) * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
@@ -404,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // still counted) of its kps K chunks, chunk-major in shared memory.
           // Fewer, larger copies: a TMA copy has a fixed cost of its own, and a
           // stage of MXFP4 blocks is only 8 KB per block.
-          uint8_t* a_s = base + p.off_a + su * (PAIR ? 16384u : 32768u);
+          uint8_t* a_s = base + p.off_a + su * p.a_slot;
           tma_load_4d(smem_u32(a_s), &tm_a, 0, 0, blk_row, (tl.e + p.e_base) * NK + ks, full);
         }
         if (!b_ready) {
@@ -413,11 +434,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int u = 0; u < kps; ++u) {
           const int kc = ks + u;
-          const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.brows * 128u);
-          if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * 128, b_row0, full);
+          const uint32_t b_s = smem_u32(base + p.off_b + (su + u) * p.brows * b_row);
+          if (lane == 0 && !gather) tma_load_2d(b_s, &tm_b, kc * kx, b_row0, full);
           __syncwarp();
           if (gather && lane < n4)
-            tma_gather4(b_s + static_cast<uint32_t>(lane) * 512u, &tm_b, kc * 128, tok[0], tok[1], tok[2],
+            tma_gather4(b_s + static_cast<uint32_t>(lane) * 4u * b_row, &tm_b, kc * kx, tok[0], tok[1], tok[2],
                         tok[3], full);
         }
         ++it;  // fills armed
@@ -476,7 +497,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t sf_base = tbase + p.sf_col0;
       const uint32_t a_base = smem_u32(base + p.off_a);
       const uint32_t b_base = smem_u32(base + p.off_b);
-      const uint32_t b_stride16 = static_cast<uint32_t>(p.brows) * (128u >> 4);
+      const uint32_t b_stride16 = (static_cast<uint32_t>(p.brows) * p.b_row) >> 4;
+      const uint32_t a16 = p.a_slot >> 4;  // A chunk slot stride in 16-byte units
+      const bool a4 = p.a4 != 0;
       const uint32_t kps = static_cast<uint32_t>(p.kps);
       // descriptors of slot 0 (start address field is addr >> 4; slots add to it)
       const uint32_t a_lo0 = desc_lo_sw128(a_base);
@@ -492,9 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d0 = tbase + ab * p.acc_cols;
         const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn);
-        uint32_t idesc[4];
+        uint32_t idesc[4], idesc4[2];
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb) idesc[kb] = idesc_mx(afmt, kFmtE4M3, kM, n_mma, kb, kb);
+        idesc4[0] = idesc_mxf4(kM, n_mma, 0);
+        idesc4[1] = idesc_mxf4(kM, n_mma, 2);
         uint32_t accum = 0u;
         for (int ks = 0; ks < NKs; ++ks) {
           const uint32_t s = rs, ph = rph;
@@ -512,9 +537,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tensor memory): the single issuing thread's work between two MMAs
           // is tensor time
           const uint32_t slot0 = s * kps;
-          constexpr uint32_t a16 = (PAIR ? 16384u : 32768u) >> 4;  // A slot stride in 16-byte units
           constexpr uint32_t sfc = PAIR ? kSfColsPerChunkPair : kSfColsPerChunk;
-          if (two) {
+          if (!PAIR && a4) {
+            for (uint32_t u = 0; u < kps; ++u) {
+              const uint32_t al = a_lo0 + (slot0 + u) * a16, bl = b_lo0 + (slot0 + u) * b_stride16;
+              const uint32_t sf = sf_base + (slot0 + u) * sfc;
+              if (two) issue_chunk_a4<true>(d0, d1, al, bl, sf, idesc4, accum);
+              else issue_chunk_a4<false>(d0, d1, al, bl, sf, idesc4, accum);
+            }
+          } else if (two) {
             issue_chunk<PAIR, true>(d0, d1, a_lo0 + slot0 * a16, b_lo0 + slot0 * b_stride16, sf_base + slot0 * sfc,
                                     idesc, accum);
             if (kps == 2)
@@ -711,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* const h_scales = p.h_scales;
         const bool act_oai = p.act != 0;
         const float alpha = p.alpha, limit = p.limit;
+        const bool h4 = p.a4 != 0;  // h re-quantised to MXFP4 (packed E2M1, I/2 bytes a row)
         // 8 columns at a time, each step over all 8 so that the per-column
         // chains (SwiGLU, warp amax, exponent, encode) overlap; the tensor-
         // memory loads of the warp's next 8 columns are in flight while the
@@ -736,6 +768,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int cc = 0; cc < 8; ++cc) u[cc] = __reduce_max_sync(0xffffffffu, u[cc]);
+          if (h4) {
+            // MXFP4: lanes 2i and 2i + 1 (rows 2i, 2i + 1 of I) share one byte,
+            // row 2i in the low nibble; per column 16 bytes through the
+            // per-warp tile [8 columns][16 bytes]
+            int my_s4 = 0;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc) {
+              const int sc = mx_block_exponent(u[cc], 2);
+              const uint32_t code = enc_e2m1(__uint_as_float(g[cc]) * pow2_neg(sc));
+              const uint32_t hi = __shfl_down_sync(0xffffffffu, code, 1);
+              if ((lane & 1) == 0) ebuf[cc * 16 + (lane >> 1)] = static_cast<uint8_t>(code | (hi << 4));
+              if (lane == cc) my_s4 = sc;
+            }
+            __syncwarp();
+            const int nv = tl.rows - c0;
+            if (lane < 8 && lane < nv) {
+              const uint4 v = *reinterpret_cast<const uint4*>(ebuf + lane * 16);
+              *reinterpret_cast<uint4*>(h_codes + static_cast<size_t>(tl.p0 + c0 + lane) * (I / 2) + i0 / 2) = v;
+              h_scales[static_cast<size_t>(tl.p0 + c0 + lane) * I32 + i0 / 32] = static_cast<uint8_t>(my_s4 + 127);
+            }
+            __syncwarp();
+            return;
+          }
           // codes go through a per-warp shared-memory tile [8 columns][32 rows
           // of I] so that each lane writes one 16-byte run of an h row (byte
           // stores from every lane, one per column, throttle the store path)
@@ -962,7 +1017,7 @@ bool pair_supported(const GemmArgs& a) {
   // each CTA of a pair takes one row block of every weight tile (so every
   // tile needs both), with token rows in slot order (2-D boxes) split in halves
   const int rows = a.epi == 0 ? 2 * a.I : a.H;
-  return !a.gather4 && (rows / 128) % 2 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
+  return !a.gather4 && !a.a4 && (rows / 128) % 2 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
@@ -1026,6 +1081,11 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.pdl = a.pdl;
   p.hint_ns = 20000u;
   if (const char* env = std::getenv("MXMOE_PAIR_HINT_NS")) p.hint_ns = static_cast<uint32_t>(std::atoi(env));
+  // packed E2M1 operands: weight blocks of 8 KB (64-byte rows) and token rows
+  // of 64 bytes per K chunk stay packed in shared memory (64-byte swizzle)
+  p.a4 = a.a4;
+  p.a_slot = pair ? 16384u : a.a4 ? 16384u : 32768u;
+  p.b_row = a.a4 ? 64u : 128u;
 
   // shared memory and tensor memory plan for `kps` 128-wide K chunks per
   // pipeline stage: returns the stage count (0 if fewer than two fit)
@@ -1039,7 +1099,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const uint32_t x_bytes = (pair && a.epi == 0) ? 128u * p.xs * 4u : 0u;
   const uint32_t fixed =
       1024u /*align slack*/ + meta_bytes + 512u /*barriers*/ + 128u /*static*/ + epi_bytes + x_bytes;
-  const uint32_t a_stage = (pair ? 16384u : 32768u);  // unpacked weight blocks per K chunk
+  const uint32_t a_stage = p.a_slot;  // weight blocks of one K chunk
   const char* env_stages = std::getenv("MXMOE_STAGES");  // tuning override (only lowers)
   auto plan = [&](int kps, int* acc_bufs, uint32_t* sf_col0) {
     // two accumulator buffers (the epilogue of one tile overlaps the next
@@ -1047,7 +1107,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     *acc_bufs = (2u * p.acc_cols + 2u * p.sfc * kps <= kTmemCols) ? 2 : 1;
     *sf_col0 = static_cast<uint32_t>(*acc_bufs) * p.acc_cols;
     if (*sf_col0 + 2u * p.sfc * kps > kTmemCols) return 0;
-    const uint32_t per_stage = (a_stage + static_cast<uint32_t>(p.brows) * 128u) * static_cast<uint32_t>(kps);
+    const uint32_t per_stage = (a_stage + static_cast<uint32_t>(p.brows) * p.b_row) * static_cast<uint32_t>(kps);
     if (static_cast<uint32_t>(max_smem) <= fixed) return 0;
     int st = static_cast<int>((static_cast<uint32_t>(max_smem) - fixed) / per_stage);
     if (st > kMaxStages) st = kMaxStages;
@@ -1070,7 +1130,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   if (const char* env = std::getenv(a.epi == 1 && std::getenv("MXMOE_KPS2") ? "MXMOE_KPS2" : "MXMOE_KPS")) {
     const int v = std::atoi(env);
-    if (v == 1 || (v == 2 && (p.K / 128) % 2 == 0)) p.kps = v;
+    // four chunks a stage only with packed E2M1 operands (whose MMA loop takes any count)
+    if (v == 1 || ((v == 2 || (v == 4 && p.a4)) && (p.K / 128) % v == 0)) p.kps = v;
   }
   const int stages = plan(p.kps, &p.acc_bufs, &p.sf_col0);
   if (stages < 2) return cudaErrorInvalidConfiguration;
@@ -1079,7 +1140,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.off_a = off;
   off += static_cast<uint32_t>(stages * p.kps) * a_stage;
   p.off_b = off;
-  off += static_cast<uint32_t>(stages * p.kps) * p.brows * 128u;
+  off += static_cast<uint32_t>(stages * p.kps) * p.brows * p.b_row;
   p.off_meta = off;
   off += meta_bytes;
   p.off_bar = off;
@@ -1097,15 +1158,17 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     // one box is a stage's row blocks (the tile's two, one per CTA of a pair)
     // of kps consecutive K chunks
     const size_t nchunk = static_cast<size_t>(a.E + 1) * p.NK;
-    cuuint64_t dims[4] = {128, 128, static_cast<cuuint64_t>(p.RB), static_cast<cuuint64_t>(nchunk)};
+    // packed E2M1 for kind::mxf4: each block 128 rows of 64 bytes, as bytes
+    const cuuint64_t inner = a.a4 ? 64 : 128;
+    cuuint64_t dims[4] = {inner, 128, static_cast<cuuint64_t>(p.RB), static_cast<cuuint64_t>(nchunk)};
     cuuint64_t strides[3];
-    cuuint32_t box[4] = {128, 128, pair ? 1u : 2u, static_cast<cuuint32_t>(p.kps)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), 128, pair ? 1u : 2u, static_cast<cuuint32_t>(p.kps)};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUtensorMapDataType dt;
     const cuuint64_t blk_bytes = a.fmt == MX_E4M3 ? 16384 : 8192;
-    if (a.fmt == MX_E4M3) {
+    if (a.fmt == MX_E4M3 || a.a4) {
       dt = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-      strides[0] = 128;
+      strides[0] = inner;
     } else {
       dt = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
       strides[0] = 64;
@@ -1113,7 +1176,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     strides[1] = blk_bytes;
     strides[2] = blk_bytes * static_cast<cuuint64_t>(p.RB);
     CUresult r = encode(&tm_a, dt, 4, const_cast<void*>(a.w_prep), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, a.a4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
@@ -1121,13 +1184,16 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     // gather4: the activation matrix [T, H], four token rows at a time (box one
     // row high); otherwise slot-ordered rows [n_rows, K], one box of `brows`
     // rows per stage (bn, or half of it for each CTA of a pair)
+    // (packed E2M1 rows: K/2 bytes, 64 per K chunk)
     const cuuint64_t b_rows = static_cast<cuuint64_t>(p.gather4 ? a.T : a.n_rows);
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(p.K), b_rows};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(p.K)};
-    cuuint32_t box[2] = {128, p.gather4 ? 1u : static_cast<cuuint32_t>(p.brows)};
+    const cuuint64_t row_bytes = a.a4 ? static_cast<cuuint64_t>(p.K / 2) : static_cast<cuuint64_t>(p.K);
+    cuuint64_t dims[2] = {row_bytes, b_rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {a.a4 ? 64u : 128u, p.gather4 ? 1u : static_cast<cuuint32_t>(p.brows)};
     cuuint32_t es[2] = {1, 1};
     CUresult r = encode(&tm_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.b_codes), dims,
-                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        a.a4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }

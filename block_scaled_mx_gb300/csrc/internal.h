@@ -9,8 +9,9 @@
 namespace mxk {
 
 // ---- prep.cu
+// x bf16 -> MX codes (fmt MX_E4M3: one byte per element; MX_E2M1: two per byte)
 cudaError_t launch_quantize_act(const void* x, int64_t n_elems, uint8_t* codes, uint8_t* scales,
-                                cudaStream_t s);
+                                cudaStream_t s, int fmt = 0 /* MX_E4M3 */);
 cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, uint8_t* codes,
                                     uint8_t* scales, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -38,7 +39,8 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
 struct PrologueArgs {
   const uint4* x;       // bf16 [T, H] as 16-byte groups
   int64_t n8;           // T*H/8
-  uint2* codes;         // MXFP8 codes, 8 per group
+  uint2* codes;         // MXFP8 codes, 8 per group (MXFP4: 4 bytes per group)
+  int act_e2m1;         // quantise to MXFP4 instead
   uint8_t* scales;
   const float* logits;
   int T, E, k;
@@ -122,6 +124,9 @@ struct GemmArgs {
   // gate/up epilogue activation: 0 SwiGLU, 1 SwiGLU-OAI with alpha and limit
   int act;
   float alpha, limit;
+  // MXFP4 weights with MXFP4 token rows (kind::mxf4): activations / h packed
+  // E2M1 ([rows, K/2] bytes), h re-quantised to MXFP4 by the gate/up epilogue
+  int a4;
 };
 bool pair_supported(const GemmArgs& a);
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);

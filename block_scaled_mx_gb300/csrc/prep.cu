@@ -65,22 +65,57 @@ __device__ __forceinline__ void quantize_act_step(const uint4* __restrict__ x, i
   }
 }
 
-__global__ void __launch_bounds__(256) k_quantize_act(const uint4* __restrict__ x, int64_t n8,
-                                                      uint2* __restrict__ codes,
+// The same for MXFP4 activations: shared exponent with emax 2 (E2M1), codes
+// packed two per byte, element 2i in the low nibble (one 32-bit word of 8 codes
+// per thread).
+__device__ __forceinline__ void quantize_act_step_e2m1(const uint4* __restrict__ x, int64_t n8, int64_t i,
+                                                       int lane, uint32_t* __restrict__ codes,
+                                                       uint8_t* __restrict__ scales) {
+  const bool valid = i < n8;
+  const uint4 v = valid ? __ldg(&x[i]) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t amax = 0;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    amax = max(amax, w[m] & 0x7FFFu);
+    amax = max(amax, (w[m] >> 16) & 0x7FFFu);
+  }
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const int s = mx_block_exponent(amax << 16, 2);
+  const float p = pow2_neg(s);
+  uint32_t packed = 0u;
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    packed |= enc_e2m1(__uint_as_float(w[m] << 16) * p) << (8 * m);
+    packed |= enc_e2m1(__uint_as_float(w[m] & 0xFFFF0000u) * p) << (8 * m + 4);
+  }
+  if (valid) {
+    codes[i] = packed;
+    if ((lane & 3) == 0) scales[i >> 2] = static_cast<uint8_t>(s + 127);
+  }
+}
+
+template <bool E2M1>
+__global__ void __launch_bounds__(256) k_quantize_act(const uint4* __restrict__ x, int64_t n8, void* __restrict__ codes,
                                                       uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i - lane < n8;
-       i += stride)
-    quantize_act_step(x, n8, i, lane, codes, scales);
+       i += stride) {
+    if (E2M1) quantize_act_step_e2m1(x, n8, i, lane, static_cast<uint32_t*>(codes), scales);
+    else quantize_act_step(x, n8, i, lane, static_cast<uint2*>(codes), scales);
+  }
 }
 
 cudaError_t launch_quantize_act(const void* x, int64_t n_elems, uint8_t* codes, uint8_t* scales,
-                                cudaStream_t s) {
+                                cudaStream_t s, int fmt) {
   const int64_t n8 = n_elems / 8;
   if (n8 == 0) return cudaSuccess;
-  k_quantize_act<<<grid_for(n8, 256, 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8,
-                                                      reinterpret_cast<uint2*>(codes), scales);
+  if (fmt == MX_E2M1)
+    k_quantize_act<true><<<grid_for(n8, 256, 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8, codes, scales);
+  else
+    k_quantize_act<false><<<grid_for(n8, 256, 8), 256, 0, s>>>(static_cast<const uint4*>(x), n8, codes, scales);
   return cudaGetLastError();
 }
 
@@ -471,7 +506,11 @@ __global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
     topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
-  for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
+  if (a.act_e2m1)
+    for (int64_t i = first; i - lane < a.n8; i += stride)
+      quantize_act_step_e2m1(a.x, a.n8, i, lane, reinterpret_cast<uint32_t*>(a.codes), a.scales);
+  else
+    for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
   for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (!PERMUTE) return;
   __threadfence();

@@ -161,6 +161,25 @@ __device__ __forceinline__ uint32_t desc_lo_sw128(uint32_t addr) {
   return ((addr >> 4) & 0x3FFFu) | (1u << 16);
 }
 constexpr uint32_t kDescHiSw128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // 128-byte swizzle
+// The same for a K-major, 64-byte-swizzled operand (rows of 64 bytes: 128
+// packed E2M1 values), 8-row groups 512 bytes apart, swizzle mode 4 (64 B).
+// The low half is desc_lo_sw128's (start address, leading byte offset).
+constexpr uint32_t kDescHiSw64 = (512u >> 4) | (1u << 14) | (4u << 29);
+
+// Block-scaled MMA with both operands packed E2M1 (kind::mxf4): K = 64 per
+// instruction, one E8M0 scale per 32 elements (scale_vec::2X: two scale bytes
+// of each row's 32-bit TMEM word per instruction); operands as mma_mxf8f6f4_lo.
+__device__ __forceinline__ void mma_mxf4_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t desc_hi,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "mov.b64 ad, {%1, %7};\n\t"
+      "mov.b64 bd, {%2, %7};\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], ad, bd, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem), "r"(desc_hi));
+}
 
 // Arrive (once) on an mbarrier when every previously issued tcgen05 async
 // operation of this thread has completed.
@@ -342,6 +361,14 @@ constexpr uint32_t kFmtE2M1 = 5;
 // Instruction descriptor for kind::mxf8f6f4 with E8M0 scales, both operands
 // K-major, dense.  M in {128}, N a multiple of 16 in [16, 256].  sfa_id/sfb_id
 // pick the byte of the 32-bit TMEM scale word that this K = 32 step uses.
+// Instruction descriptor for kind::mxf4 (both operands E2M1, format code 1 in
+// this kind), E8M0 scales, K-major, dense; sf_id (0 or 2) picks the pair of
+// scale bytes of each row's TMEM word that this K = 64 step uses.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t sf_id) {
+  return ((sf_id & 3u) << 4) | (1u << 7) | (1u << 10) | (((N >> 3) & 0x3Fu) << 17) | (1u << 23) |
+         (((M >> 4) & 0x1Fu) << 24) | ((sf_id & 3u) << 29);
+}
+
 __host__ __device__ __forceinline__ uint32_t idesc_mx(uint32_t a_fmt, uint32_t b_fmt, uint32_t M,
                                                       uint32_t N, uint32_t sfa_id,
                                                       uint32_t sfb_id) {

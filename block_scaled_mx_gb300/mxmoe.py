@@ -51,6 +51,7 @@ _P, _I, _I64, _SZ, _U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.
 SIGNATURES = {
     "mx_status_string": (ctypes.c_char_p, [_I]),
     "mx_quantize_act": (_I, [_P, _I, _I, _P, _P, _P]),
+    "mx_quantize_act_ex": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "mx_quantize_weights": (_I, [_P, _I64, _I, _I, _P, _P, _P]),
     "moe_route_topk": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "moe_route_gemm_topk": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P]),
@@ -62,6 +63,7 @@ SIGNATURES = {
     "moe_gemm_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_grouped_gemm_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _SZ, _P]),
     "moe_grouped_gemm_down_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
+    "moe_grouped_gemm_down_combine_ex": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
     "moe_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_forward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P]),
     "moe_forward_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P, _P]),
@@ -140,9 +142,15 @@ def _fmt(fmt) -> int:
 
 
 # ------------------------------------------------------------------ step calls
-def mx_quantize_act(x, codes, scales, stream=None):
+def mx_quantize_act(x, codes, scales, stream=None, fmt=None):
+    """x bf16 [T, H] -> MX codes and E8M0 scales; fmt None/"e4m3" (codes [T, H])
+    or "e2m1" (MXFP4, codes [T, H/2])."""
     T, H = x.shape
-    _check(lib().mx_quantize_act(_ptr(x), T, H, _ptr(codes), _ptr(scales), _stream(stream)), "mx_quantize_act")
+    if fmt is None:
+        _check(lib().mx_quantize_act(_ptr(x), T, H, _ptr(codes), _ptr(scales), _stream(stream)), "mx_quantize_act")
+    else:
+        _check(lib().mx_quantize_act_ex(_ptr(x), T, H, _fmt(fmt), _ptr(codes), _ptr(scales), _stream(stream)),
+               "mx_quantize_act_ex")
 
 
 def mx_quantize_weights(w, fmt, codes, scales, stream=None):
@@ -218,11 +226,19 @@ def moe_grouped_gemm_swiglu_ex(act_codes, act_scales, offsets, sorted_slot, w1_p
 
 
 def moe_grouped_gemm_down_combine(h_codes, h_scales, offsets, sorted_slot, topk_w, w2_prep, fmt, T, H, I, E, k,
-                                  out, ws, stream=None):
-    _check(lib().moe_grouped_gemm_down_combine(_ptr(h_codes), _ptr(h_scales), _ptr(offsets), _ptr(sorted_slot),
-                                               _ptr(topk_w), _ptr(w2_prep), _fmt(fmt), T, H, I, E, k, _ptr(out),
-                                               _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
-           "moe_grouped_gemm_down_combine")
+                                  out, ws, stream=None, opts=None):
+    if opts is None:
+        _check(lib().moe_grouped_gemm_down_combine(_ptr(h_codes), _ptr(h_scales), _ptr(offsets), _ptr(sorted_slot),
+                                                   _ptr(topk_w), _ptr(w2_prep), _fmt(fmt), T, H, I, E, k, _ptr(out),
+                                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+               "moe_grouped_gemm_down_combine")
+    else:
+        _check(lib().moe_grouped_gemm_down_combine_ex(_ptr(h_codes), _ptr(h_scales), _ptr(offsets),
+                                                      _ptr(sorted_slot), _ptr(topk_w), _ptr(w2_prep), _fmt(fmt), T,
+                                                      H, I, E, k, _ptr(out), _ptr(ws),
+                                                      ws.numel() * ws.element_size(), _opts_ptr(opts),
+                                                      _stream(stream)),
+               "moe_grouped_gemm_down_combine_ex")
 
 
 def moe_workspace_size(T, H, I, E, k, fmt) -> int:

@@ -90,6 +90,14 @@ MX_API const char* mx_status_string(int status);
 MX_API int mx_quantize_act(const void* x_bf16, int T, int H, uint8_t* codes, uint8_t* scales,
                     mx_stream_t stream);
 
+/* mx_quantize_act to a chosen MX format: fmt MX_E4M3 (as mx_quantize_act) or
+ * MX_E2M1 (MXFP4: emax 2, codes [T, H/2] bytes, element 2i in the low nibble,
+ * saturation at 6), scales [T, H/32].  Errors as mx_quantize_act, plus
+ * MX_ERR_INVALID_ARG for another fmt.  Source: as mx_quantize_act; MXFP4
+ * activations are the mx_layer_opts act_fmt variant. */
+MX_API int mx_quantize_act_ex(const void* x_bf16, int T, int H, int fmt, uint8_t* codes, uint8_t* scales,
+                              mx_stream_t stream);
+
 /* Weight quantisation, fp32 -> MXFP8 or MXFP4 (load-time helper; same rule as
  * mx_quantize_act with emax 8 for E4M3 and 2 for E2M1, saturation at 6 for
  * E2M1).  w [rows, K] fp32; codes [rows, K] (E4M3) or [rows, K/2] (E2M1);
@@ -231,6 +239,7 @@ MX_API int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* 
                                   int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                                   mx_stream_t stream);
 
+
 /* Bytes of workspace moe_forward needs (intermediates + GEMM scratch). */
 MX_API size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt);
 
@@ -266,8 +275,15 @@ MX_API int moe_forward_launches(int T, int H, int I, int E, int k, int fmt);
  *    GEMM pair covers routed and shared experts) or MX_SHARED_DENSE (the path
  *    that figure replaces: the shared expert runs as its own dense gate/up and
  *    down launches after the routed ones; same arithmetic, two more launches).
- *  - act_fmt: MX_E4M3 (MXFP8 activations and h); MX_E2M1 is reserved for
- *    MXFP4 activations (MX_ERR_UNSUPPORTED where not built). */
+ *  - act_fmt: MX_E4M3 (MXFP8 activations and h) or MX_E2M1 (MXFP4
+ *    activations and h: x and h are quantised to E2M1 with an E8M0 scale per
+ *    32 elements, emax 2, and both grouped GEMMs run on the packed-FP4 MMA
+ *    with MXFP4 weights on both sides).  MX_E2M1 needs fmt == MX_E2M1
+ *    (MX_ERR_UNSUPPORTED with MXFP8 weights).  The activation codes
+ *    (and h codes) are then [rows, K/2] bytes, element 2i in the low nibble.
+ *    Source: the MI355X page's opening results list (an MXFP4 model) and its
+ *    passage on native MX back ends; the element and scale rule is OCP MX
+ *    v1.0's for E2M1. */
 typedef struct mx_layer_opts {
   int activation;
   float alpha;
@@ -283,13 +299,23 @@ MX_API int moe_forward_ex(const void* x_bf16, const float* logits, const void* w
                           int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                           const mx_layer_opts* opts, mx_stream_t stream);
 
-/* moe_grouped_gemm_swiglu with layer options (the activation is used; the
- * other fields must hold their defaults). */
+/* moe_grouped_gemm_swiglu with layer options (the activation and act_fmt are
+ * used: with MX_E2M1 the activation codes are MXFP4 [T, H/2] bytes and h is
+ * written as MXFP4, [rows, I/2] bytes; shared_expert must be folded). */
 MX_API int moe_grouped_gemm_swiglu_ex(const uint8_t* act_codes, const uint8_t* act_scales,
                                       const int32_t* offsets, const int32_t* sorted_slot, const void* w1_prep,
                                       int fmt, int T, int H, int I, int E, int k, uint8_t* h_codes,
                                       uint8_t* h_scales, void* ws, size_t ws_bytes, const mx_layer_opts* opts,
                                       mx_stream_t stream);
+
+/* moe_grouped_gemm_down_combine with layer options: act_fmt MX_E2M1 reads
+ * MXFP4 h ([rows, I/2] bytes; needs MXFP4 weights); the other fields must hold
+ * their defaults' kind (the activation is not used here). */
+MX_API int moe_grouped_gemm_down_combine_ex(const uint8_t* h_codes, const uint8_t* h_scales,
+                                            const int32_t* offsets, const int32_t* sorted_slot,
+                                            const float* topk_w, const void* w2_prep, int fmt, int T, int H,
+                                            int I, int E, int k, float* out, void* ws, size_t ws_bytes,
+                                            const mx_layer_opts* opts, mx_stream_t stream);
 
 /* Kernel launches moe_forward_ex enqueues for this shape and these options
  * (host only; -1 for a rejected shape or option). */

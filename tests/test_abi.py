@@ -129,7 +129,7 @@ def test_forward_launch_count(L):
 
 def test_layer_options_are_checked_on_the_host(L):
     """mx_layer_opts: unknown values and a non-positive clamp limit are invalid
-    arguments; MXFP4 activations are not available through this call; the
+    arguments; MXFP4 activations with MXFP8 weights are unsupported; the
     dense shared-expert variant adds two launches."""
     from block_scaled_mx_gb300 import mxmoe as mx
 
@@ -141,9 +141,15 @@ def test_layer_options_are_checked_on_the_host(L):
         assert L.moe_forward_ex(fake, fake, fake, fake, 0, 4, 256, 128, 8, 2, fake, fake, 1 << 30, ctypes.addressof(o),
                                 None) == mx.MX_ERR_INVALID_ARG
         assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, ctypes.addressof(o)) == -1
+    # MXFP4 activations need MXFP4 weights (the packed-FP4 MMA takes E2M1 on both sides)
     fp4 = mx.layer_opts(act_fmt="e2m1")
-    assert L.moe_forward_ex(fake, fake, fake, fake, 1, 4, 256, 128, 8, 2, fake, fake, 1 << 30,
+    assert L.moe_forward_ex(fake, fake, fake, fake, 0, 4, 256, 128, 8, 2, fake, fake, 1 << 30,
                             ctypes.addressof(fp4), None) == mx.MX_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_swiglu_ex(fake, fake, fake, fake, fake, 0, 4, 256, 128, 8, 2, fake, fake, fake,
+                                        1 << 30, ctypes.addressof(fp4), None) == mx.MX_ERR_UNSUPPORTED
+    assert L.moe_grouped_gemm_down_combine_ex(fake, fake, fake, fake, fake, fake, 0, 4, 256, 128, 8, 2, fake, fake,
+                                              1 << 30, ctypes.addressof(fp4), None) == mx.MX_ERR_UNSUPPORTED
+    assert L.mx_quantize_act_ex(fake, 4, 256, 7, fake, fake, None) == mx.MX_ERR_INVALID_ARG
     dense = mx.layer_opts(shared="dense")
     assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, ctypes.addressof(dense)) == 5
     assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, None) == 3

@@ -458,3 +458,88 @@ def test_dense_shared_expert_with_swiglu_oai():
     assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
     rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
     assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+
+
+# ---- MXFP4 activations (kind::mxf4: both operands packed E2M1)
+@pytest.mark.parametrize("T,H", [(1, 32), (16, 256), (37, 4096), (6, 2048), (4096, 4096)])
+def test_quantize_act_e2m1_bitexact(T, H):
+    """x bf16 -> MXFP4 codes (two per byte, element 2i low) and E8M0 scales,
+    bit-exact against the oracle's quantiser (emax 2, RNE, saturate at 6);
+    special blocks as in the MXFP8 case."""
+    x = _bf16(T, H, 11)
+    if T >= 16:
+        x[0, :32] = 0.0
+        x[1, :32] = -0.0
+        x[2, :32] = 1e-39
+        x[3, :32] = 3.0e38
+    codes = torch.empty(T, H // 2, dtype=torch.uint8, device="cuda")
+    scales = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
+    mx.mx_quantize_act(x.cuda(), codes, scales, fmt="e2m1")
+    rc, rs = oracle.quantize_bf16(W.bf16_bits(x), oracle.E2M1)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def _nibbles(c):
+    c = c.astype(np.int64)
+    return np.stack([c & 15, c >> 4], axis=-1).reshape(c.shape[0], -1)
+
+
+A4_CASES = ["decode_mxfp4", "specverify_mxfp4", "ragged_e2m1", "wide_e2m1", "one_expert", "max_routing"]
+
+
+@pytest.mark.parametrize("name", A4_CASES)
+def test_mxfp4_activations_layer_parity(name):
+    """MXFP4 activations and h on the packed-FP4 MMA against the oracle run
+    with the same MXFP4 quantisation of x and h: activation codes bit-exact,
+    h codes equal but for rare one-step flips at rounding boundaries, the
+    layer output within the same tolerance as the MXFP8 layer (the oracle does
+    the same quantisations; the GPU accumulates in fp32).  The variant's output
+    differs from the MXFP8-activation layer by far more than that tolerance."""
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ref = oracle.moe_forward(L.x_bits, L.logits_np, k, L.o1c, L.o1s, L.o2c, L.o2s, L.fmt, I, want_h=True,
+                             act_fmt=oracle.E2M1)
+    opts = mx.layer_opts(act_fmt="e2m1")
+    # step-wise calls
+    act_c = torch.empty(T, H // 2, dtype=torch.uint8, device="cuda")
+    act_s = torch.empty(T, H // 32, dtype=torch.uint8, device="cuda")
+    mx.mx_quantize_act(L.x, act_c, act_s, fmt="e2m1")
+    assert np.array_equal(act_c.cpu().numpy(), ref["act_codes"])
+    assert np.array_equal(act_s.cpu().numpy(), ref["act_scales"])
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    mx.moe_route_topk(L.logits, k, ids, w)
+    counts = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 2, dtype=torch.int32, device="cuda")
+    ss = torch.empty(T * (k + 1), dtype=torch.int32, device="cuda")
+    pws = mx.alloc_workspace(mx.moe_permute_workspace_size(T, E, k))
+    mx.moe_permute(ids, E, counts, offsets, ss, pws)
+    gws = mx.alloc_workspace(mx.moe_gemm_workspace_size(T, H, I, E, k))
+    h_c = torch.empty(T * (k + 1), I // 2, dtype=torch.uint8, device="cuda")
+    h_s = torch.empty(T * (k + 1), I // 32, dtype=torch.uint8, device="cuda")
+    mx.moe_grouped_gemm_swiglu_ex(act_c, act_s, offsets, ss, L.layer.w1, L.fmt, T, H, I, E, k, h_c, h_s, gws, opts)
+    out = torch.zeros(T, H, dtype=torch.float32, device="cuda")
+    mx.moe_grouped_gemm_down_combine(h_c, h_s, offsets, ss, w, L.layer.w2, L.fmt, T, H, I, E, k, out, gws, opts=opts)
+    assert (mx.moe_get_status(pws), mx.moe_get_status(gws)) == (0, 0)
+    srt = ss.cpu().numpy()
+    gc, gs = h_c.cpu().numpy(), h_s.cpu().numpy()
+    rc, rs = ref["h_codes"][srt], ref["h_scales"][srt]
+    assert np.all(np.abs(gs.astype(np.int64) - rs.astype(np.int64)) <= 1), "a block scale moved by more than one"
+    gv = oracle.decode_matrix(gc, gs, oracle.E2M1)
+    rv = oracle.decode_matrix(rc, rs, oracle.E2M1)
+    frac = np.count_nonzero(_nibbles(gc) != _nibbles(rc)) / (gc.size * 2)
+    hrel = np.linalg.norm(gv - rv) / np.linalg.norm(rv)
+    print(f"MXFP4 h codes {name}: mismatch fraction {frac:.2e}, decoded rel L2 {hrel:.2e}")
+    assert frac < 0.005 and hrel < 0.02, (frac, hrel)
+    rel, mabs = out_errors(out.double().cpu().numpy(), ref["out"])
+    assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    # the fused single call
+    fused = L.layer.forward(L.x, L.logits, opts=opts)
+    assert mx.moe_get_status(L.layer.workspace(T)) == 0
+    rel2, mabs2 = out_errors(fused.double().cpu().numpy(), ref["out"])
+    assert rel2 <= OUT_REL_L2 and mabs2 <= OUT_MAX_ABS_OVER_RMS, (rel2, mabs2)
+    # a different layer from the MXFP8-activation one
+    std = oracle_forward(L)["out"]
+    assert np.linalg.norm(ref["out"] - std) > 4 * OUT_REL_L2 * np.linalg.norm(std)
