@@ -190,6 +190,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     float thr = -INFINITY;  // the k-th best score so far
     const uint32_t lane_base = tbase + (static_cast<uint32_t>(32 * q) << 16);
+    // each thread's 16 logits of a column chunk go through its own 64 bytes of
+    // shared memory (the pipeline stages are idle by now), so the selection
+    // below runs as one rolled loop: one copy of its code, fetched once
+    float* const mine = reinterpret_cast<float*>(base) + (static_cast<size_t>(tid) - 64) * 16;
     for (int c0 = 0; ok && c0 < p.n_pad; c0 += 16) {
       uint32_t v[16];
       __syncwarp();
@@ -203,10 +207,14 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
       if (!p.ids) continue;
 #pragma unroll
+      for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(mine + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                           __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+#pragma unroll 1
       for (int i = 0; i < 16; ++i) {
         const int e = c0 + i;
         if (e >= E) break;
-        const float logit = __uint_as_float(v[i]);
+        const float logit = mine[i];
         const float score = logit + (p.bias ? __ldg(&p.bias[e]) : 0.0f);
         if (score > thr) {
           // insertion into the descending list: the candidate goes in front
