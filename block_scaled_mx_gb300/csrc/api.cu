@@ -79,6 +79,14 @@ int forward_launches(int T, int E, int k, bool dense_shared = false) {
   const bool wide = wide_schedule(T, E, k);
   const bool fused = T <= kPermuteChunk && !wide;
   const int nchunks = (T + kPermuteChunk - 1) / kPermuteChunk;
+  if (!fused) {
+    // the one-launch prologue of a large batch, when its grid fits on this GPU
+    PrologueArgs pa{};
+    pa.T = T;
+    pa.E = E;
+    pa.k = k;
+    if (prologue_big_blocks(pa) > 0) return 1 + (dense_shared ? 4 : 2);
+  }
   return 1 + (fused ? 0 : (nchunks > 1 ? 2 : 1)) + (wide ? 1 : 0) + (dense_shared ? 4 : 2);
 }
 
@@ -96,6 +104,7 @@ struct ForwardWs {
   uint8_t* act_sorted;
   uint8_t* h_codes;
   uint8_t* h_scales;
+  unsigned* gbar;  // grid-barrier counter of the large-batch prologue
   size_t bytes;
 };
 
@@ -121,6 +130,7 @@ ForwardWs carve_forward(void* ws, int T, int H, int I, int E, int k) {
   f.act_sorted = take(gather_bytes(T, H, E, k));
   f.h_codes = take(slots * I);
   f.h_scales = take(slots * (I / 32));
+  f.gbar = reinterpret_cast<unsigned*>(take(4));
   f.bytes = off;
   return f;
 }
@@ -174,7 +184,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   GemmArgs a{};
   a.bn = choose_bn(T, E, k, 0);
   a.gather4 = a.bn <= 64 ? 1 : 0;
-  a.pdl = a.gather4 ? pdl : 0;
+  a.pdl = pdl;
   a.a4 = lo.act_fmt == MX_E2M1 ? 1 : 0;
   a.act = lo.act;
   a.alpha = lo.alpha;
@@ -464,12 +474,32 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
   pa.offsets = f.offsets;
   pa.sorted_slot = f.sorted_slot;
   pa.sc = f.perm;
-  if (launch_prologue(pa, s) != cudaSuccess) return MX_ERR_CUDA;
-  if (!fused && launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
-    return MX_ERR_CUDA;
+  // A batch larger than one permutation chunk (or on the wide schedule) runs
+  // its whole prologue, chunked permutation and row gather included, as one
+  // grid-synchronised launch when the grid fits on the GPU at once; else as
+  // separate launches.
+  const bool wide = wide_schedule(T, E, k);
+  const int big_blocks = fused ? 0 : prologue_big_blocks(pa);
+  const bool big = big_blocks > 0;
+  if (big) {
+    BigPrologueArgs b{};
+    b.bar = f.gbar;
+    b.gathered = wide ? f.act_sorted : nullptr;
+    b.row_bytes = lo.act_fmt == MX_E2M1 ? H / 2 : H;
+    b.wait_limit_ns = g_wait_limit_ns;
+    if (launch_prologue_big(pa, b, big_blocks, s) != cudaSuccess) return MX_ERR_CUDA;
+  } else {
+    if (launch_prologue(pa, s) != cudaSuccess) return MX_ERR_CUDA;
+    if (!fused && launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
+      return MX_ERR_CUDA;
+  }
+  // the gate/up GEMM follows the prologue directly (programmatic dependent
+  // launch) unless separate permutation launches came in between
+  const int pdl1 = (fused || big) ? 1 : 0;
+  const bool gather = !big;  // the wide schedule's row gather, unless the prologue did it
   if (lo.shared == MX_SHARED_FOLDED) {
     st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                   f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0, lo);
+                   f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, pdl1, lo, Window(), gather);
     if (st != MX_OK) return st;
     return run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E,
                      k, out, f.perm.status, s, 2, Window(), lo.act_fmt == MX_E2M1 ? 1 : 0);
@@ -483,10 +513,10 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
   shared.n = 1;
   shared.e_base = E;
   st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 1 : 0, lo, routed);
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, pdl1, lo, routed, gather);
   if (st != MX_OK) return st;
   st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,
-                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, fused ? 2 : 0, lo, shared, false);
+                 f.h_codes, f.h_scales, f.perm.status, f.act_sorted, s, pdl1 ? 2 : 0, lo, shared, false);
   if (st != MX_OK) return st;
   st = run_gemm2(f.h_codes, f.h_scales, f.offsets, f.sorted_slot, f.topk_w, w2_prep, fmt, T, H, I, E, k, out,
                  f.perm.status, s, 2, routed, lo.act_fmt == MX_E2M1 ? 1 : 0);

@@ -55,6 +55,17 @@ struct PrologueArgs {
   PermuteScratch sc;
 };
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
+// The prologue of a batch larger than one permutation chunk in one launch:
+// routing, quantisation, zeroing, the chunked permutation and (gathered set)
+// the activation rows in slot order, phases separated by grid barriers.
+struct BigPrologueArgs {
+  unsigned* bar;            // grid-barrier counter (zeroed by the launch)
+  uint8_t* gathered;        // [T*(k+1), row_bytes] slot-ordered activation rows, or null
+  int64_t row_bytes;        // bytes of one activation row (H, or H/2 for MXFP4)
+  unsigned long long wait_limit_ns;
+};
+int prologue_big_blocks(const PrologueArgs& a);  // 0: not possible on this GPU
+cudaError_t launch_prologue_big(const PrologueArgs& a, const BigPrologueArgs& b, int blocks, cudaStream_t s);
 
 // dst[p, :] = src[sorted_slot[p] / (k+1), :] for p < n_rows (rows of `row_bytes`).
 cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,

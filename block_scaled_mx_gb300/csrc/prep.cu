@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace mxk {
 
@@ -547,6 +548,148 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   kern<<<g, kPermuteChunk, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ prologue of a large batch
+// The first launch of the layer for T > kPermuteChunk: one grid whose blocks
+// are all resident at once (its size comes from the occupancy query) runs, with
+// a grid barrier (a global counter, bounded waits) between the phases:
+//   0. routing (warp per token), quantisation of x, zeroing of out;
+//   1. the chunked permutation's first pass, one block per chunk of 256
+//      tokens, the last of them (counter, nobody waits) turning the per-chunk
+//      counts into the expert offsets and chunk bases;
+//   2. the scatter of every slot to its position;
+//   3. (wide schedule) the copy of each slot's activation row into slot
+//      order, the B operand the wide gate/up GEMM loads as 2-D boxes.
+// Together with the two grouped GEMMs the layer is then three launches.
+namespace {
+__device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, unsigned long long limit_ns) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    int ok = 1;
+    const uint64_t t0 = globaltimer_ns();
+    while (*reinterpret_cast<volatile unsigned*>(bar) < target) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        set_status(status, MX_ERR_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(128);
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+}  // namespace
+
+template <int PER>
+__global__ void __launch_bounds__(kPermuteChunk) k_prologue_big(PrologueArgs a, BigPrologueArgs b) {
+  extern __shared__ uint32_t bits[];
+  // the GEMM after this grid waits for its completion (griddepcontrol.wait) and
+  // may set up meanwhile
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned G = gridDim.x;
+  // phase 0
+  for (int t = blockIdx.x * (kPermuteChunk / 32) + warp; t < a.T; t += gridDim.x * (kPermuteChunk / 32))
+    topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
+  if (a.act_e2m1)
+    for (int64_t i = first; i - lane < a.n8; i += stride)
+      quantize_act_step_e2m1(a.x, a.n8, i, lane, reinterpret_cast<uint32_t*>(a.codes), a.scales);
+  else
+    for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
+  for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!grid_barrier(b.bar, G, a.sc.status, b.wait_limit_ns)) return;
+  // phase 1: counting pass, offsets and chunk bases (last chunk block)
+  const int nchunks = (a.T + kPermuteChunk - 1) / kPermuteChunk;
+  if (static_cast<int>(blockIdx.x) < nchunks)
+    permute_count_block(a.ids, a.T, a.E, a.k, a.counts, a.offsets, a.sorted_slot, a.sc, nchunks, blockIdx.x, bits);
+  if (!grid_barrier(b.bar, 2 * G, a.sc.status, b.wait_limit_ns)) return;
+  // phase 2: scatter (as k_permute_scatter; the counters are reset for the next call)
+  if (static_cast<int>(blockIdx.x) < nchunks) {
+    const int chunk = blockIdx.x;
+    const int t = chunk * kPermuteChunk + tid;
+    if (blockIdx.x == 0 && tid == 0) *a.sc.done = 0u;
+    if (t < a.T) {
+      for (int j = 0; j < a.k; ++j) {
+        const int e = __ldcg(&a.ids[static_cast<int64_t>(t) * a.k + j]);
+        if (e < 0 || e >= a.E) continue;
+        const int pos = __ldcg(&a.sc.chunk_base[static_cast<int64_t>(chunk) * a.E + e]) +
+                        __ldcg(&a.sc.local_rank[static_cast<int64_t>(t) * a.k + j]);
+        a.sorted_slot[pos] = t * (a.k + 1) + j;
+      }
+      a.sorted_slot[__ldcg(&a.offsets[a.E]) + t] = t * (a.k + 1) + a.k;
+    }
+  }
+  if (b.gathered == nullptr) return;
+  if (!grid_barrier(b.bar, 3 * G, a.sc.status, b.wait_limit_ns)) return;
+  // phase 3: activation rows in slot order (16-byte units; written above by
+  // other blocks, so read through L2)
+  // four independent copies in flight per thread (each a slot load, then a
+  // row load, then a store)
+  const int64_t row_chunks = b.row_bytes / 16;
+  const int64_t total = row_chunks * static_cast<int64_t>(a.T) * (a.k + 1);
+  const uint4* __restrict__ src = reinterpret_cast<const uint4*>(a.codes);
+  uint4* __restrict__ dst = reinterpret_cast<uint4*>(b.gathered);
+  const int32_t* __restrict__ ss = a.sorted_slot;
+  for (int64_t i0 = first; i0 < total; i0 += 4 * stride) {
+    int tt[4];
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      tt[u] = i < total ? __ldcg(&ss[i / row_chunks]) / (a.k + 1) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < total && tt[u] >= 0 && tt[u] < a.T) v[u] = __ldcg(&src[static_cast<int64_t>(tt[u]) * row_chunks + i % row_chunks]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i >= total) continue;
+      if (tt[u] < 0 || tt[u] >= a.T) set_status(a.sc.status, MX_ERR_DEVICE_ARG);
+      else dst[i] = v[u];
+    }
+  }
+}
+
+// Blocks of the large-batch prologue that fit on the GPU at once (0: none).
+int prologue_big_blocks(const PrologueArgs& a) {
+  const size_t smem = permute_block_smem(a.T, a.E, a.k);
+  void (*kern)(PrologueArgs, BigPrologueArgs) = a.E <= 32 ? k_prologue_big<1> : a.E <= 128 ? k_prologue_big<4>
+                                               : a.E <= 512 ? k_prologue_big<16> : k_prologue_big<32>;
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kPermuteChunk, smem) != cudaSuccess) return 0;
+  if (per_sm > 8) per_sm = 8;
+  const int nchunks = (a.T + kPermuteChunk - 1) / kPermuteChunk;
+  const int blocks = per_sm * sm_count();
+  return blocks >= nchunks ? blocks : 0;
+}
+
+cudaError_t launch_prologue_big(const PrologueArgs& a, const BigPrologueArgs& b, int blocks, cudaStream_t s) {
+  const size_t smem = permute_block_smem(a.T, a.E, a.k);
+  void (*kern)(PrologueArgs, BigPrologueArgs) = a.E <= 32 ? k_prologue_big<1> : a.E <= 128 ? k_prologue_big<4>
+                                               : a.E <= 512 ? k_prologue_big<16> : k_prologue_big<32>;
+  // the barrier counter and the permutation's last-block counter start at
+  // zero (memsets, not kernels; the latter also after an earlier call that
+  // stopped half-way)
+  cudaError_t e = cudaMemsetAsync(b.bar, 0, sizeof(unsigned), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(a.sc.done, 0, sizeof(unsigned), s);
+  if (e != cudaSuccess) return e;
+  kern<<<static_cast<unsigned>(blocks), kPermuteChunk, smem, s>>>(a, b);
   return cudaGetLastError();
 }
 

@@ -244,7 +244,13 @@ MX_API int moe_grouped_gemm_down_combine(const uint8_t* h_codes, const uint8_t* 
 MX_API size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt);
 
 /* The whole layer in one call, no host synchronisation: quantise, route,
- * permute, both grouped GEMMs; out [T, H] fp32 is overwritten.
+ * permute, both grouped GEMMs; out [T, H] fp32 is overwritten.  Three kernel
+ * launches: a prologue (routing, quantisation, zeroing of out, the
+ * permutation and, on the wide schedule, the activation rows in slot order;
+ * for more than 256 tokens its phases are separated by grid barriers, plus
+ * two 4-byte memsets of its counters) and the two grouped GEMMs as
+ * programmatically dependent launches.  A batch whose prologue grid would not
+ * fit on the GPU at once falls back to separate permutation launches.
  * Errors: union of the step calls.
  * Source: the MI355X page, the passage on launch cost and graph execution and
  * Figure 4's passage (removing launches and intermediate traffic raised output
@@ -254,8 +260,9 @@ MX_API int moe_forward(const void* x_bf16, const float* logits, const void* w1_p
                 int fmt, int T, int H, int I, int E, int k, float* out, void* ws, size_t ws_bytes,
                 mx_stream_t stream);
 
-/* Number of kernel launches moe_forward enqueues for this shape (host only;
- * -1 for a shape moe_forward rejects, 0 for T = 0). */
+/* Number of kernel launches moe_forward enqueues for this shape on the
+ * current device (host only: no kernel runs; -1 for a shape moe_forward
+ * rejects, 0 for T = 0). */
 MX_API int moe_forward_launches(int T, int H, int I, int E, int k, int fmt);
 
 /* ---- layer variants ---- */
