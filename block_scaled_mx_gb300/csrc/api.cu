@@ -79,7 +79,8 @@ int forward_launches(int T, int E, int k, bool dense_shared = false) {
   const bool wide = wide_schedule(T, E, k);
   const bool fused = T <= kPermuteChunk && !wide;
   const int nchunks = (T + kPermuteChunk - 1) / kPermuteChunk;
-  if (!fused) {
+  const char* sep = std::getenv("MXMOE_SEPARATE_PERMUTE");
+  if (!fused && !(sep && sep[0] == '1')) {
     // the one-launch prologue of a large batch, when its grid fits on this GPU
     PrologueArgs pa{};
     pa.T = T;
@@ -479,7 +480,9 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
   // grid-synchronised launch when the grid fits on the GPU at once; else as
   // separate launches.
   const bool wide = wide_schedule(T, E, k);
-  const int big_blocks = fused ? 0 : prologue_big_blocks(pa);
+  // (MXMOE_SEPARATE_PERMUTE=1 forces the separate launches: A/B runs, tests)
+  const char* sep = std::getenv("MXMOE_SEPARATE_PERMUTE");
+  const int big_blocks = (fused || (sep && sep[0] == '1')) ? 0 : prologue_big_blocks(pa);
   const bool big = big_blocks > 0;
   if (big) {
     BigPrologueArgs b{};

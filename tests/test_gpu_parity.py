@@ -328,6 +328,29 @@ def test_forward_graph_capture(name):
     assert err < 1e-5, err
 
 
+@pytest.mark.parametrize("name", ["ragged_e4m3", "wide_e4m3", "wide_e2m1", "pair_e4m3"])
+def test_large_batch_prologue_matches_separate_launches(name, monkeypatch):
+    """Batches above one permutation chunk (or on the wide schedule): the
+    one-launch prologue (grid barriers between routing, counting, scatter and
+    row gather) gives the layer of the separate permutation and gather
+    launches, and the oracle's."""
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    assert mx.moe_forward_launches(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt) == 3
+    ref = oracle_forward(L)
+    one = L.layer.forward(L.x, L.logits).clone()
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    monkeypatch.setenv("MXMOE_SEPARATE_PERMUTE", "1")
+    assert mx.moe_forward_launches(wl.T, wl.H, wl.I, wl.E, wl.k, wl.fmt) > 3
+    sep = L.layer.forward(L.x, L.logits)
+    assert mx.moe_get_status(L.layer.workspace(wl.T)) == 0
+    for got in (one, sep):
+        rel, mabs = out_errors(got.double().cpu().numpy(), ref["out"])
+        assert rel <= OUT_REL_L2 and mabs <= OUT_MAX_ABS_OVER_RMS, (rel, mabs)
+    diff = (one - sep).abs().max().item() / sep.abs().max().item()
+    assert diff < 1e-5, diff
+
+
 @pytest.mark.parametrize("name,kps", [("tiny", "2"), ("decode_mxfp8", "2"), ("decode_mxfp4", "1")])
 def test_layer_parity_other_stage_shape(name, kps, monkeypatch):
     """The narrow schedule with the other number of K chunks per pipeline stage."""
