@@ -67,8 +67,14 @@ void choose_pair(GemmArgs& a) {
 // kernel) so that each stage's 128 token rows arrive as one TMA box.
 bool wide_schedule(int T, int E, int k) { return choose_bn(T, E, k, 0) > 64; }
 
+// The wide schedule's slot-ordered activation rows (H bytes each) followed by
+// their scales K-chunk-major (H/128 words per row).
 size_t gather_bytes(int T, int H, int E, int k) {
-  return wide_schedule(T, E, k) ? al256(static_cast<size_t>(T) * (k + 1) * H) : 0;
+  const size_t slots = static_cast<size_t>(T) * (k + 1);
+  return wide_schedule(T, E, k) ? al256(slots * H) + al256(slots * (H / 32)) : 0;
+}
+uint32_t* gathered_scales(uint8_t* act_sorted, int T, int H, int k) {
+  return reinterpret_cast<uint32_t*>(act_sorted + al256(static_cast<size_t>(T) * (k + 1) * H));
 }
 
 // Kernel launches moe_forward enqueues for a shape (mirrors its branches):
@@ -193,8 +199,9 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.n_exp = win.n;
   a.e_base = win.e_base;
   if (!a.gather4 && gather_rows) {
-    if (launch_gather_rows(act_codes, T, a.a4 ? H / 2 : H, sorted_slot, k, n_rows, act_sorted, status, s) !=
-        cudaSuccess)
+    if (launch_gather_rows(act_codes, T, a.a4 ? H / 2 : H, sorted_slot, k, n_rows, act_sorted,
+                           reinterpret_cast<const uint32_t*>(act_scales), H / 128,
+                           gathered_scales(act_sorted, T, H, k), status, s) != cudaSuccess)
       return MX_ERR_CUDA;
   }
   a.epi = 0;
@@ -208,6 +215,7 @@ int run_gemm1(const uint8_t* act_codes, const uint8_t* act_scales, const int32_t
   a.b_codes = a.gather4 ? act_codes : act_sorted;
   a.n_rows = n_rows;
   a.b_scales = act_scales;
+  a.b_scales_t = a.gather4 ? nullptr : gathered_scales(act_sorted, T, H, k);
   a.offsets = offsets + win.e_base;
   a.sorted_slot = sorted_slot;
   a.h_codes = h_codes;
@@ -489,6 +497,8 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
     b.bar = f.gbar;
     b.gathered = wide ? f.act_sorted : nullptr;
     b.row_bytes = lo.act_fmt == MX_E2M1 ? H / 2 : H;
+    b.gathered_scales = wide ? gathered_scales(f.act_sorted, T, H, k) : nullptr;
+    b.scale_words = H / 128;
     b.wait_limit_ns = g_wait_limit_ns;
     if (launch_prologue_big(pa, b, big_blocks, s) != cudaSuccess) return MX_ERR_CUDA;
   } else {
@@ -496,9 +506,13 @@ int moe_forward_ex(const void* x_bf16, const float* logits, const void* w1_prep,
     if (!fused && launch_permute(f.ids, T, E, k, f.counts, f.offsets, f.sorted_slot, f.perm, s) != cudaSuccess)
       return MX_ERR_CUDA;
   }
-  // the gate/up GEMM follows the prologue directly (programmatic dependent
-  // launch) unless separate permutation launches came in between
-  const int pdl1 = (fused || big) ? 1 : 0;
+  // At decode sizes the gate/up GEMM follows the prologue as a programmatic
+  // dependent launch and lets the down GEMM launch early (its CTAs take SMs
+  // as gate/up CTAs finish and stream their first weight stages).  On the
+  // large-batch path the gate/up GEMM starts after the prologue completes and
+  // the down GEMM after the gate/up GEMM: there the early down CTAs made the
+  // 8192-token layer ~100 us slower (1.93 against 1.82 ms).
+  const int pdl1 = fused ? 1 : 0;
   const bool gather = !big;  // the wide schedule's row gather, unless the prologue did it
   if (lo.shared == MX_SHARED_FOLDED) {
     st = run_gemm1(f.act_codes, f.act_scales, f.offsets, f.sorted_slot, w1_prep, fmt, T, H, I, E, k,

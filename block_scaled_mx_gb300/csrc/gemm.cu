@@ -80,6 +80,7 @@ struct GemmParams {
   uint32_t a_tx;
   const uint8_t* w_scales;
   const uint8_t* b_scales;
+  const uint32_t* b_scales_t;  // gathered rows' scales K-chunk-major [K/128][n_rows], or null
   const int32_t* offsets;
   const int32_t* sorted_slot;
   const float* topk_w;
@@ -250,7 +251,8 @@ __device__ __forceinline__ void issue_chunk_a4(uint32_t d0, uint32_t d1, uint32_
 // (rank 1's TMA loads, scale-staging and epilogue warps arrive on them
 // remotely); the MMA commits free the stage and signal the accumulator in both
 // CTAs at once.
-template <bool PAIR>
+// BT: the token-row scales are K-chunk-major (gathered rows, b_scales_t).
+template <bool PAIR, bool BT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
@@ -598,7 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* const status = p.status;
     const uint32_t col0 = tbase + (static_cast<uint32_t>(32 * q) << 16) + p.sf_col0;
     const uint4* const wsc = reinterpret_cast<const uint4*>(p.w_scales);
-    const uint32_t* const bsc = reinterpret_cast<const uint32_t*>(p.b_scales);
+    // token-row scales: by row ([rows][K/128] words, the word of chunk kc at
+    // +kc), or K-chunk-major for gathered rows ([K/128][n_rows], at +kc n_rows:
+    // a chunk's words of consecutive rows are adjacent, one coalesced load)
+    const uint32_t* const bsc = BT ? p.b_scales_t : reinterpret_cast<const uint32_t*>(p.b_scales);
     uint32_t rs = 0, rph = 0;
     bool ok = true;
     if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -614,7 +619,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 8; ++j) {
         const int r = 32 * j + lane;
         roww[j] = -1;
-        if (r < tl.rows) {
+        if (BT && r < tl.rows) {
+          roww[j] = tl.p0 + r;
+        } else if (!BT && r < tl.rows) {
           int src_row = tl.p0 + r;
           if (p.epi == 0) {
             src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
@@ -639,8 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       auto load = [&](ScaleBuf& b, int kc) {
+        if (BT) {
+          const uint32_t* const bk = bsc + static_cast<size_t>(kc) * static_cast<size_t>(p.n_rows);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bsc + roww[j] + kc) : 0x7F7F7F7Fu;
+          for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bk + roww[j]) : 0x7F7F7F7Fu;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) b.bw[j] = roww[j] >= 0 ? __ldg(bsc + roww[j] + kc) : 0x7F7F7F7Fu;
+        }
         const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + blk_row) * 32;
         b.a0 = __ldg(blk + lane);
         b.a1 = two ? __ldg(blk + 32 + lane) : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
@@ -1069,6 +1082,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const PreparedLayout L = prepared_layout(a.E + 1, rows, p.K, a.fmt, a.epi == 0 ? 1 : 0);
   p.w_scales = static_cast<const uint8_t*>(a.w_prep) + L.scales_offset;
   p.b_scales = a.b_scales;
+  p.b_scales_t = a.b_scales_t;
   p.offsets = a.offsets;
   p.sorted_slot = a.sorted_slot;
   p.topk_w = a.topk_w;
@@ -1198,12 +1212,15 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
 
-  auto kernel = pair ? k_grouped_gemm<true> : k_grouped_gemm<false>;
+  const bool bt = a.b_scales_t != nullptr;
+  auto kernel = pair ? (bt ? k_grouped_gemm<true, true> : k_grouped_gemm<true, false>)
+                     : (bt ? k_grouped_gemm<false, true> : k_grouped_gemm<false, false>);
   // the shared-memory opt-in is per device and kernel and only ever raised:
   // skip the driver call when a launch on this device already allowed this much
   {
-    static std::atomic<int> smem_allowed[2][kMaxDevices];
-    std::atomic<int>* allowed = (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[pair ? 1 : 0][dev] : nullptr;
+    static std::atomic<int> smem_allowed[4][kMaxDevices];
+    std::atomic<int>* allowed =
+        (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[(pair ? 2 : 0) + (bt ? 1 : 0)][dev] : nullptr;
     if (!allowed || allowed->load(std::memory_order_relaxed) < static_cast<int>(smem)) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;

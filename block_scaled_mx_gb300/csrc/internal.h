@@ -62,14 +62,20 @@ struct BigPrologueArgs {
   unsigned* bar;            // grid-barrier counter (zeroed by the launch)
   uint8_t* gathered;        // [T*(k+1), row_bytes] slot-ordered activation rows, or null
   int64_t row_bytes;        // bytes of one activation row (H, or H/2 for MXFP4)
+  uint32_t* gathered_scales;  // [H/128][T*(k+1)] their scales, K-chunk-major (with gathered)
+  int64_t scale_words;      // H/128: 32-bit scale words of one activation row
   unsigned long long wait_limit_ns;
 };
 int prologue_big_blocks(const PrologueArgs& a);  // 0: not possible on this GPU
 cudaError_t launch_prologue_big(const PrologueArgs& a, const BigPrologueArgs& b, int blocks, cudaStream_t s);
 
-// dst[p, :] = src[sorted_slot[p] / (k+1), :] for p < n_rows (rows of `row_bytes`).
+// dst[p, :] = src[sorted_slot[p] / (k+1), :] for p < n_rows (rows of `row_bytes`),
+// and the rows' scales K-chunk-major: dst_sc[c * n_rows + p] = word c of scale
+// row sorted_slot[p] / (k+1) of src_sc ([T, scale_words] 32-bit words, one per
+// 128-element K chunk).
 cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
                                const int32_t* sorted_slot, int k, int n_rows, uint8_t* dst,
+                               const uint32_t* src_sc, int64_t scale_words, uint32_t* dst_sc,
                                int* status, cudaStream_t s);
 
 // Kernel layout of one weight table (see gemm.cu): codes in 128-row x
@@ -113,6 +119,8 @@ struct GemmArgs {
   int gather4;
   int n_rows;               // T*(k+1)
   const uint8_t* b_scales;  // GEMM1: act scales [T, H/32] by token; GEMM2: h scales [rows, I/32]
+  const uint32_t* b_scales_t;  // GEMM1 on gathered rows: their scales K-chunk-major
+                               // [H/128][n_rows] (one word per row and chunk), or null
   const int32_t* offsets;   // [E+2]
   const int32_t* sorted_slot;
   const float* topk_w;      // GEMM2

@@ -561,7 +561,8 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
 //      counts into the expert offsets and chunk bases;
 //   2. the scatter of every slot to its position;
 //   3. (wide schedule) the copy of each slot's activation row into slot
-//      order, the B operand the wide gate/up GEMM loads as 2-D boxes.
+//      order, the B operand the wide gate/up GEMM loads as 2-D boxes, and of
+//      its scales into K-chunk-major order.
 // Together with the two grouped GEMMs the layer is then three launches.
 namespace {
 __device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, unsigned long long limit_ns) {
@@ -587,6 +588,33 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, int* status, unsign
   return s_ok != 0;
 }
 }  // namespace
+
+// Scale words of slot-ordered rows, K-chunk-major (the grouped GEMM's scale
+// warps then read a chunk's words of consecutive rows in one coalesced load):
+// dst_sc[c * n_rows + p] = src_sc[t * words + c], t the token of slot position p.
+// A work item is one slot and a run of 8 words (consecutive items: consecutive
+// slots, so a warp's stores of one word are one 128-byte run); two loads in
+// flight per thread keep the register count of the kernels it sits in.
+__device__ __forceinline__ void gather_scales_t(const uint32_t* __restrict__ src_sc, int T, int words,
+                                                const int32_t* __restrict__ sorted_slot, int k, int n_rows,
+                                                uint32_t* __restrict__ dst_sc, int64_t first, int64_t stride) {
+  const int64_t items = static_cast<int64_t>(n_rows) * ((words + 7) / 8);
+  for (int64_t i = first; i < items; i += stride) {
+    const int g = static_cast<int>(i / n_rows);
+    const int p = static_cast<int>(i - static_cast<int64_t>(g) * n_rows);
+    const int t = __ldcg(&sorted_slot[p]) / (k + 1);
+    const bool ok = t >= 0 && t < T;
+    const uint32_t* row = src_sc + static_cast<int64_t>(ok ? t : 0) * words;
+    const int c1 = min(8 * g + 8, words);
+#pragma unroll 1
+    for (int c = 8 * g; c < c1; c += 2) {
+      const uint32_t v0 = ok ? __ldcg(row + c) : 0x7F7F7F7Fu;
+      const uint32_t v1 = (ok && c + 1 < c1) ? __ldcg(row + c + 1) : 0x7F7F7F7Fu;
+      dst_sc[static_cast<int64_t>(c) * n_rows + p] = v0;
+      if (c + 1 < c1) dst_sc[static_cast<int64_t>(c + 1) * n_rows + p] = v1;
+    }
+  }
+}
 
 template <int PER>
 __global__ void __launch_bounds__(kPermuteChunk) k_prologue_big(PrologueArgs a, BigPrologueArgs b) {
@@ -661,6 +689,9 @@ __global__ void __launch_bounds__(kPermuteChunk) k_prologue_big(PrologueArgs a, 
       else dst[i] = v[u];
     }
   }
+  if (b.gathered_scales)
+    gather_scales_t(reinterpret_cast<const uint32_t*>(a.scales), a.T, static_cast<int>(b.scale_words), ss, a.k,
+                    a.T * (a.k + 1), b.gathered_scales, first, stride);
 }
 
 // Blocks of the large-batch prologue that fit on the GPU at once (0: none).
@@ -698,10 +729,11 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
                                                      int64_t row_chunks,
                                                      const int32_t* __restrict__ sorted_slot, int k,
                                                      int64_t total_chunks, uint4* __restrict__ dst,
-                                                     int* status) {
+                                                     const uint32_t* __restrict__ src_sc, int64_t scale_words,
+                                                     uint32_t* __restrict__ dst_sc, int* status) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_chunks;
-       i += stride) {
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (int64_t i = first; i < total_chunks; i += stride) {
     const int64_t p = i / row_chunks, c = i - p * row_chunks;
     const int t = __ldg(&sorted_slot[p]) / (k + 1);
     if (t < 0 || t >= T) {
@@ -710,17 +742,22 @@ __global__ void __launch_bounds__(256) k_gather_rows(const uint4* __restrict__ s
     }
     dst[i] = __ldg(&src[static_cast<int64_t>(t) * row_chunks + c]);
   }
+  if (dst_sc)
+    gather_scales_t(src_sc, T, static_cast<int>(scale_words), sorted_slot, k,
+                    static_cast<int>(total_chunks / row_chunks), dst_sc, first, stride);
 }
 
 cudaError_t launch_gather_rows(const uint8_t* src, int T, int64_t row_bytes,
                                const int32_t* sorted_slot, int k, int n_rows, uint8_t* dst,
+                               const uint32_t* src_sc, int64_t scale_words, uint32_t* dst_sc,
                                int* status, cudaStream_t s) {
   const int64_t row_chunks = row_bytes / 16;
   const int64_t total = row_chunks * n_rows;
   if (total == 0) return cudaSuccess;
   k_gather_rows<<<grid_for(total, 256, 8), 256, 0, s>>>(reinterpret_cast<const uint4*>(src), T,
                                                         row_chunks, sorted_slot, k, total,
-                                                        reinterpret_cast<uint4*>(dst), status);
+                                                        reinterpret_cast<uint4*>(dst), src_sc, scale_words,
+                                                        dst_sc, status);
   return cudaGetLastError();
 }
 

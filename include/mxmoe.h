@@ -248,9 +248,9 @@ MX_API size_t moe_workspace_size(int T, int H, int I, int E, int k, int fmt);
  * launches: a prologue (routing, quantisation, zeroing of out, the
  * permutation and, on the wide schedule, the activation rows in slot order;
  * for more than 256 tokens its phases are separated by grid barriers, plus
- * two 4-byte memsets of its counters) and the two grouped GEMMs as
- * programmatically dependent launches.  A batch whose prologue grid would not
- * fit on the GPU at once falls back to separate permutation launches.
+ * two 4-byte memsets of its counters) and the two grouped GEMMs (up to 256
+ * tokens as programmatically dependent launches).  A batch whose prologue grid
+ * would not fit on the GPU at once falls back to separate permutation launches.
  * Errors: union of the step calls.
  * Source: the MI355X page, the passage on launch cost and graph execution and
  * Figure 4's passage (removing launches and intermediate traffic raised output
