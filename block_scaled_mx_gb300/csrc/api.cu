@@ -596,6 +596,10 @@ int moe_get_status(void* ws, mx_stream_t stream, int* host_status) {
 
 void mx_debug_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns = ns; }
 
+void mx_debug_time_gemms(int enable) { gemm_timing_enable(enable != 0); }
+
+int mx_debug_gemm_times(float* ms, int* epi, int max) { return gemm_timing_read(ms, epi, max < 0 ? 0 : max); }
+
 #ifndef MXMOE_BUILD_STAMP
 #define MXMOE_BUILD_STAMP "unstamped"
 #endif

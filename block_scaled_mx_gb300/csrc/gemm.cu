@@ -40,6 +40,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -1033,6 +1034,69 @@ bool pair_supported(const GemmArgs& a) {
   return !a.gather4 && !a.a4 && (rows / 128) % 2 == 0 && a.bn % 32 == 0 && a.bn >= 32 && a.bn <= 256;
 }
 
+// ---- optional per-launch timing (mx_debug_time_gemms)
+namespace {
+constexpr int kMaxTimed = 4096;
+struct GemmTimer {
+  std::mutex m;
+  bool on = false;
+  int dev = -1;  // device of the events (set at the first recorded launch)
+  int n = 0;
+  cudaEvent_t ev[kMaxTimed][2] = {};
+  int epi[kMaxTimed] = {};
+};
+GemmTimer& gemm_timer() {
+  static GemmTimer t;
+  return t;
+}
+// the slot to record this launch into (-1: not timing, full or another device)
+int timer_begin(int epi, cudaStream_t s) {
+  GemmTimer& t = gemm_timer();
+  std::lock_guard<std::mutex> g(t.m);
+  if (!t.on || t.n >= kMaxTimed) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (t.dev < 0) t.dev = dev;
+  if (dev != t.dev) return -1;
+  const int i = t.n;
+  for (int j = 0; j < 2; ++j)
+    if (!t.ev[i][j] && cudaEventCreate(&t.ev[i][j]) != cudaSuccess) return -1;
+  if (cudaEventRecord(t.ev[i][0], s) != cudaSuccess) return -1;
+  t.epi[i] = epi;
+  ++t.n;
+  return i;
+}
+void timer_end(int i, cudaStream_t s) {
+  if (i < 0) return;
+  GemmTimer& t = gemm_timer();
+  std::lock_guard<std::mutex> g(t.m);
+  cudaEventRecord(t.ev[i][1], s);
+}
+}  // namespace
+
+void gemm_timing_enable(bool on) {
+  GemmTimer& t = gemm_timer();
+  std::lock_guard<std::mutex> g(t.m);
+  t.on = on;
+  t.n = 0;
+}
+
+int gemm_timing_read(float* ms, int* epi, int max) {
+  GemmTimer& t = gemm_timer();
+  std::lock_guard<std::mutex> g(t.m);
+  const int n = t.n;
+  int rc = n;
+  for (int i = 0; i < n && i < max; ++i) {
+    float v = 0.f;
+    if (cudaEventSynchronize(t.ev[i][1]) != cudaSuccess || cudaEventElapsedTime(&v, t.ev[i][0], t.ev[i][1]) != cudaSuccess)
+      rc = -1;
+    if (ms) ms[i] = v;
+    if (epi) epi[i] = t.epi[i];
+  }
+  t.n = 0;
+  return rc;
+}
+
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
@@ -1233,9 +1297,12 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   int units = sm_count_gemm() / (pair ? 2 : 1);
   if (bound < units) units = static_cast<int>(bound > 0 ? bound : 1);
   const int grid = units * (pair ? 2 : 1);
+  const int timed = timer_begin(a.epi, stream);
   if (!a.pdl && !pair) {
     kernel<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    timer_end(timed, stream);
+    return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1258,7 +1325,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kernel, p, tm_a, tm_b);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p, tm_a, tm_b);
+  timer_end(timed, stream);
+  return e;
 }
 
 }  // namespace mxk

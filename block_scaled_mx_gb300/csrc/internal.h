@@ -148,6 +148,10 @@ struct GemmArgs {
   int a4;
 };
 bool pair_supported(const GemmArgs& a);
+// Per-launch timing of the grouped GEMM kernels (mx_debug_time_gemms).
+void gemm_timing_enable(bool on);
+int gemm_timing_read(float* ms, int* epi, int max);
+
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t s);
 
 }  // namespace mxk

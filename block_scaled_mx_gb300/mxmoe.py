@@ -72,6 +72,8 @@ SIGNATURES = {
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I, _I]),
     "moe_get_status": (_I, [_P, _P, _P]),
     "mx_debug_set_wait_limit_ns": (None, [_U64]),
+    "mx_debug_time_gemms": (None, [_I]),
+    "mx_debug_gemm_times": (_I, [_P, _P, _I]),
     "mx_build_stamp": (ctypes.c_char_p, []),
 }
 
@@ -278,6 +280,23 @@ def moe_get_status(ws, stream=None) -> int:
 
 def mx_debug_set_wait_limit_ns(ns: int):
     lib().mx_debug_set_wait_limit_ns(int(ns))
+
+
+def mx_debug_time_gemms(enable: bool):
+    """Start (or stop) bracketing each grouped-GEMM launch with CUDA events."""
+    lib().mx_debug_time_gemms(1 if enable else 0)
+
+
+def mx_debug_gemm_times(max_n: int = 4096):
+    """Device times (ms) and epilogues (0 gate/up, 1 down) of the grouped-GEMM
+    launches recorded since timing was enabled or last read; clears them."""
+    ms = (ctypes.c_float * max_n)()
+    epi = (ctypes.c_int * max_n)()
+    n = lib().mx_debug_gemm_times(ctypes.cast(ms, _P), ctypes.cast(epi, _P), max_n)
+    if n < 0:
+        raise MxError(MX_ERR_CUDA, "mx_debug_gemm_times")
+    n = min(n, max_n)
+    return [float(ms[i]) for i in range(n)], [int(epi[i]) for i in range(n)]
 
 
 def mx_build_stamp() -> str:

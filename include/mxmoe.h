@@ -337,6 +337,20 @@ MX_API int moe_get_status(void* ws, mx_stream_t stream, int* host_status);
  * exercises the MX_ERR_TIMEOUT path without hanging the GPU. */
 MX_API void mx_debug_set_wait_limit_ns(uint64_t ns);
 
+/* Measurement hook: while enabled (enable != 0), each grouped-GEMM kernel
+ * launch is bracketed by two CUDA events the library records on the launch's
+ * stream (the first 4096 launches after enabling; events of the device that is
+ * current at the first recorded launch, later launches on another device are
+ * not recorded).  mx_debug_gemm_times waits for the recorded events, writes for
+ * the first min(n, max) launches the kernel's device time in milliseconds
+ * (ms[i]) and its epilogue (epi[i]: 0 gate/up, 1 down), forgets them and
+ * returns n, the number recorded (-1: a CUDA error).  Enabling or disabling
+ * also forgets them.  Not for streams being captured into a CUDA graph.  The
+ * pages have no counterpart: it times the dominant kernel apart from the row
+ * gather that shares its call. */
+MX_API void mx_debug_time_gemms(int enable);
+MX_API int mx_debug_gemm_times(float* ms, int* epi, int max);
+
 /* Hash of the sources, flags and compiler this library was built from
  * (16 hex digits; static string).  Lets a caller check that the library it
  * loaded was compiled from the sources it expects. */

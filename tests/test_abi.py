@@ -154,3 +154,14 @@ def test_layer_options_are_checked_on_the_host(L):
     assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, ctypes.addressof(dense)) == 5
     assert L.moe_forward_launches_ex(32, 4096, 1536, 128, 8, 0, None) == 3
     assert mx.moe_forward_launches_ex(32, 4096, 1536, 128, 8, "e4m3", mx.layer_opts("swiglu_oai")) == 3
+
+
+def test_gemm_timing_hook_without_launches(L):
+    """The timing hook makes no CUDA call until a GEMM launch is recorded:
+    enabling, reading (nothing recorded) and disabling work without a GPU."""
+    from block_scaled_mx_gb300 import mxmoe as mx
+
+    mx.mx_debug_time_gemms(True)
+    assert mx.mx_debug_gemm_times() == ([], [])
+    mx.mx_debug_time_gemms(False)
+    assert L.mx_debug_gemm_times(None, None, 0) == 0

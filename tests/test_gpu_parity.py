@@ -566,3 +566,27 @@ def test_mxfp4_activations_layer_parity(name):
     # a different layer from the MXFP8-activation one
     std = oracle_forward(L)["out"]
     assert np.linalg.norm(ref["out"] - std) > 4 * OUT_REL_L2 * np.linalg.norm(std)
+
+
+@pytest.mark.parametrize("name", ["tiny", "wide_e4m3"])
+def test_gemm_launch_timing_hook(name):
+    """mx_debug_time_gemms brackets each grouped-GEMM launch with events: the
+    step-wise layer records one gate/up and one down launch with positive
+    device times (the wide schedule's row gather is not inside them), reading
+    clears them, and nothing is recorded while timing is off."""
+    wl = LAYER_CASES[name]
+    L = build_layer(wl)
+    mx.mx_debug_time_gemms(True)
+    try:
+        r = _steps(L)
+        torch.cuda.synchronize()
+        ms, epi = mx.mx_debug_gemm_times()
+        assert epi == [0, 1], epi
+        assert all(0.0 < t < 1000.0 for t in ms), ms
+        assert mx.mx_debug_gemm_times() == ([], [])
+    finally:
+        mx.mx_debug_time_gemms(False)
+    assert r["status"] == (0, 0)
+    _steps(L)
+    torch.cuda.synchronize()
+    assert mx.mx_debug_gemm_times() == ([], [])
