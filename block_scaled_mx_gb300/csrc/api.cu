@@ -38,9 +38,12 @@ int choose_bn(int T, int E, int k, int which) {
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
   if (mean_rows < 12.0) return 16;  // smaller B tiles leave room for a third stage
   if (mean_rows < 48.0) return 32;
-  // down GEMM: two accumulator buffers at 96 rows hide its atomic-combine
-  // epilogue behind the next tile's MMAs, which beats the fewer MMAs of 192
-  return which == 0 ? 192 : 96;
+  // down GEMM: 192 rows with one W2 row block a tile (M = 128) keeps two
+  // accumulator buffers (the atomic-combine epilogue overlaps the next tile's
+  // MMAs) with MMAs of N = 192, past the per-instruction issue floor of
+  // narrower ones (the 8192-token layer: 0.67 ms against 0.71 ms for two row
+  // blocks and 96 rows)
+  return 192;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
@@ -254,6 +257,10 @@ int run_gemm2(const uint8_t* h_codes, const uint8_t* h_scales, const int32_t* of
   a.pdl = pdl;
   a.a4 = a4;
   a.bn = choose_bn(T, E, k, 1);
+  // wide tiles take one W2 row block each (two accumulator buffers fit); MXFP4
+  // activations keep two row blocks of 96 rows
+  if (a4 && a.bn > 96) a.bn = 96;
+  a.one_blk = (!a4 && a.bn >= 128) ? 1 : 0;
   a.wait_limit_ns = g_wait_limit_ns;
   choose_pair(a);
   return cuda_status(launch_grouped_gemm(a, s));

@@ -102,6 +102,8 @@ struct GemmParams {
   int a4;           // both operands packed E2M1 (kind::mxf4): MXFP4 activations and h
   uint32_t a_slot;  // shared-memory bytes of one K chunk of weight blocks
   uint32_t b_row;   // shared-memory bytes of one token row of one K chunk (128, or 64 packed E2M1)
+  int one;          // down GEMM, single CTA: one W2 row block per tile (M = 128), for wide token
+                    // tiles with two accumulator buffers
 };
 
 struct Tile {
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
       // the tile's first prepared row block (a pair's CTA: its own block)
-      const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
+      const int blk_row = p.one ? tl.m : 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
       // a pair's MMA takes token rows [0, N/2) from rank 0 and [N/2, N) from
       // rank 1, N the tile's rows rounded up to 16
       int n_mma = (tl.rows + 15) & ~15;
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_row = p.b_row;
       const int kx = p.a4 ? 64 : 128;  // bytes of a K chunk in a token row
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 4u * b_row : static_cast<uint32_t>(p.brows) * b_row;
-      const uint32_t bytes = ((PAIR ? 1u : 2u) * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
+      const uint32_t bytes = ((PAIR || p.one ? 1u : 2u) * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
         const uint32_t s = rs, ph = rph;
         if (!warp_wait_bar<PAIR>(sh, &sh.empty[s], ph ^ 1u, lim, status)) {
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = unit0; t < total && ok; t += unit_step) {
         const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-        const bool two = !PAIR && (p.epi == 0 || (2 * tl.m + 1 < p.RB));
+        const bool two = !PAIR && !p.one && (p.epi == 0 || (2 * tl.m + 1 < p.RB));
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
         if (!wait_bar<PAIR>(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
@@ -611,8 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = unit0; t < total && ok; t += unit_step) {
       const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
       // the tile's first prepared row block (a pair's CTA: its own, the only one)
-      const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
-      const bool two = !PAIR && 2 * tl.m + 1 < p.RB;
+      const int blk_row = p.one ? tl.m : 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
+      const bool two = !PAIR && !p.one && 2 * tl.m + 1 < p.RB;
       // rows 32j + lane of this tile: the word offset of their scale rows
       // (-1: a padding row)
       int roww[8];
@@ -905,9 +907,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         }
       } else {
-        // W2 row blocks 2m and 2m + 1 (a pair's CTA: its own one)
-        const int blk_row = 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
-        const bool two = !PAIR && 2 * tl.m + 1 < p.RB;
+        // W2 row blocks 2m and 2m + 1 (a pair's CTA: its own one; one block a tile: m)
+        const int blk_row = p.one ? tl.m : 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
+        const bool two = !PAIR && !p.one && 2 * tl.m + 1 < p.RB;
         float* const out = p.out;
         const int H = p.H;
         float* const ebf = reinterpret_cast<float*>(ebuf);
@@ -1121,7 +1123,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.RB = rows / 128;
   // weight tiles of two row blocks (gate and up block m, or W2 blocks 2m and
   // 2m + 1); a CTA pair splits each tile's two blocks between its CTAs
-  p.NM = a.epi == 0 ? a.I / 128 : (p.RB + 1) / 2;
+  // one row block per tile: the down GEMM on wide token tiles (MXFP8 operands)
+  p.one = (a.epi == 1 && !pair && !a.a4 && a.one_blk) ? 1 : 0;
+  p.NM = a.epi == 0 ? a.I / 128 : p.one ? p.RB : (p.RB + 1) / 2;
   // down GEMM: split the weight tiles into groups so that one group's slice of
   // `out` (T rows x the group's 256-column blocks, fp32) stays within ~16 MB of
   // L2 while every expert's atomic combine lands on it
@@ -1139,7 +1143,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   p.bn = a.bn;
   p.brows = pair ? a.bn / 2 : a.bn;
   p.sfc = pair ? kSfColsPerChunkPair : kSfColsPerChunk;
-  p.acc_cols = (pair ? 1u : 2u) * static_cast<uint32_t>(a.bn);
+  p.acc_cols = (pair || p.one ? 1u : 2u) * static_cast<uint32_t>(a.bn);
   p.xs = static_cast<uint32_t>(a.bn / 2 + 4);
   p.n_rows = a.n_rows;
   p.a_tx = weight_block_tx_bytes(a.fmt);
@@ -1162,7 +1166,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   // packed E2M1 operands: weight blocks of 8 KB (64-byte rows) and token rows
   // of 64 bytes per K chunk stay packed in shared memory (64-byte swizzle)
   p.a4 = a.a4;
-  p.a_slot = pair ? 16384u : a.a4 ? 16384u : 32768u;
+  p.a_slot = (pair || p.one) ? 16384u : a.a4 ? 16384u : 32768u;
   p.b_row = a.a4 ? 64u : 128u;
 
   // shared memory and tensor memory plan for `kps` 128-wide K chunks per
@@ -1206,6 +1210,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     uint32_t sc;
     if (plan(2, &ab, &sc) >= 2) p.kps = 2;
   }
+  // one row block a tile: single-chunk stages (five in flight at 192 rows
+  // measured ahead of two double-chunk stages)
+  if (p.one) p.kps = 1;
   if (const char* env = std::getenv(a.epi == 1 && std::getenv("MXMOE_KPS2") ? "MXMOE_KPS2" : "MXMOE_KPS")) {
     const int v = std::atoi(env);
     // four chunks a stage only with packed E2M1 operands (whose MMA loop takes any count)
@@ -1240,7 +1247,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
     const cuuint64_t inner = a.a4 ? 64 : 128;
     cuuint64_t dims[4] = {inner, 128, static_cast<cuuint64_t>(p.RB), static_cast<cuuint64_t>(nchunk)};
     cuuint64_t strides[3];
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), 128, pair ? 1u : 2u, static_cast<cuuint32_t>(p.kps)};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), 128, (pair || p.one) ? 1u : 2u, static_cast<cuuint32_t>(p.kps)};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUtensorMapDataType dt;
     const cuuint64_t blk_bytes = a.fmt == MX_E4M3 ? 16384 : 8192;

@@ -137,6 +137,9 @@ struct GemmArgs {
   // run as clusters of two CTAs with the pair MMA (M = 256 over two SMs; each
   // SM loads half of the token rows); needs pair_supported()
   int pair;
+  // down GEMM: one W2 row block per tile (M = 128) instead of two, so that a
+  // wide token tile still has two accumulator buffers
+  int one_blk;
   // expert window: this launch covers n_exp experts (0: all E + 1), table
   // experts e_base .. e_base + n_exp - 1; `offsets` then points at entry e_base
   int n_exp, e_base;
