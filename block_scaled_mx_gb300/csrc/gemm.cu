@@ -255,7 +255,13 @@ __device__ __forceinline__ void issue_chunk_a4(uint32_t d0, uint32_t d1, uint32_
 // remotely); the MMA commits free the stage and signal the accumulator in both
 // CTAs at once.
 // BT: the token-row scales are K-chunk-major (gathered rows, b_scales_t).
-template <bool PAIR, bool BT>
+// EPI: 0 gate/up (SwiGLU + requantisation), 1 down (weighted combine), -1
+// either (p.epi).  The wide schedule's launches take the specialised kernels
+// (smaller code: 2% on the 8192-token layer).  The narrow schedule's two
+// launches share one kernel (-1): the down launch's CTAs start as the gate/up
+// CTAs leave, and with the gate/up launch's code still in the caches; with a
+// kernel of its own the 16-token layer was 7 us slower (its code fetched cold).
+template <bool PAIR, bool BT, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
@@ -513,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = unit0; t < total && ok; t += unit_step) {
         const Tile tl = decode_tile(t, sh, E1 - 1, p.MG, p.bn, per_group);
-        const bool two = !PAIR && !p.one && (p.epi == 0 || (2 * tl.m + 1 < p.RB));
+        const bool two = !PAIR && !p.one && (EPI == 0 || (EPI < 0 && p.epi == 0) || (2 * tl.m + 1 < p.RB));
         uint32_t n_mma = static_cast<uint32_t>((tl.rows + 15) & ~15);
         if (n_mma < 16) n_mma = 16;
         if (!wait_bar<PAIR>(sh, &sh.acc_empty[ab], aph ^ 1u, lim, status)) break;
@@ -626,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           roww[j] = tl.p0 + r;
         } else if (!BT && r < tl.rows) {
           int src_row = tl.p0 + r;
-          if (p.epi == 0) {
+          if (EPI == 0 || (EPI < 0 && p.epi == 0)) {
             src_row = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
             if (src_row < 0 || src_row >= p.T) {
               set_status(status, MX_ERR_DEVICE_ARG);
@@ -733,7 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ epilogue
     const int q = warp & 3;                   // TMEM lane quarter of this warp
     const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks
-    uint8_t* const ebuf = base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(p.epi);
+    uint8_t* const ebuf =
+        base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(EPI < 0 ? p.epi : EPI);
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
     uint32_t ab = 0, aph = 0, ab_next = 0, aph_next = 0;
     uint32_t xph = 0;  // pair gate/up: phase of the exchange barriers
@@ -751,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
       const uint32_t d0 = tbase + lane_base + ab * p.acc_cols;
       const uint32_t d1 = d0 + static_cast<uint32_t>(p.bn);
-      if (p.epi == 0) {
+      if (EPI == 0 || (EPI < 0 && p.epi == 0)) {
         const int i0 = tl.m * 128 + 32 * q;  // this warp's 32 rows of I (one MX block of h)
         const int I = p.I, I32 = p.I / 32;
         uint8_t* const h_codes = p.h_codes;
@@ -1284,14 +1291,18 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   }
 
   const bool bt = a.b_scales_t != nullptr;
-  auto kernel = pair ? (bt ? k_grouped_gemm<true, true> : k_grouped_gemm<true, false>)
-                     : (bt ? k_grouped_gemm<false, true> : k_grouped_gemm<false, false>);
+  const bool narrow = a.bn <= 64 && !pair && !bt;
+  void (*kernel)(GemmParams, CUtensorMap, CUtensorMap) =
+      narrow ? k_grouped_gemm<false, false, -1>
+      : a.epi == 0 ? (pair ? (bt ? k_grouped_gemm<true, true, 0> : k_grouped_gemm<true, false, 0>)
+                           : (bt ? k_grouped_gemm<false, true, 0> : k_grouped_gemm<false, false, 0>))
+                   : (pair ? k_grouped_gemm<true, false, 1> : k_grouped_gemm<false, false, 1>);
   // the shared-memory opt-in is per device and kernel and only ever raised:
   // skip the driver call when a launch on this device already allowed this much
   {
-    static std::atomic<int> smem_allowed[4][kMaxDevices];
-    std::atomic<int>* allowed =
-        (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[(pair ? 2 : 0) + (bt ? 1 : 0)][dev] : nullptr;
+    static std::atomic<int> smem_allowed[7][kMaxDevices];
+    const int which = narrow ? 6 : a.epi == 0 ? (pair ? 2 : 0) + (bt ? 1 : 0) : 4 + (pair ? 1 : 0);
+    std::atomic<int>* allowed = (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[which][dev] : nullptr;
     if (!allowed || allowed->load(std::memory_order_relaxed) < static_cast<int>(smem)) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
       if (e != cudaSuccess) return e;
