@@ -419,7 +419,8 @@ def measure_variants(args, layer, wl, x, logits, flush, stream, dev, folded_us, 
     w_r = (torch.randn(wl.E, wl.H, generator=g, device=dev) / wl.H ** 0.5).to(torch.bfloat16)
     ids = torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev)
     tw = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
-    rws = mx.alloc_workspace(256, dev)
+    # room for the logits: batches of up to 128 tokens then take the small-batch kernel
+    rws = mx.alloc_workspace(256 + 4 * wl.T * wl.E, dev)
     for _ in range(args.warmup):
         mx.moe_route_gemm_topk(x, w_r, wl.k, rws, topk_ids=ids, topk_w=tw)
     torch.cuda.synchronize()

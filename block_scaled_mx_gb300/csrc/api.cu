@@ -575,6 +575,11 @@ int moe_route_gemm_topk(const void* x_bf16, const void* w_router_bf16, const flo
   a.topk_w = topk_w;
   a.status = static_cast<int*>(ws);
   a.wait_limit_ns = g_wait_limit_ns;
+  // the small-batch kernel's block counter (the workspace's second word) and,
+  // when the caller keeps no logits, room for them past the first 256 bytes
+  a.counter = static_cast<unsigned*>(ws) + 1;
+  if (!logits && ws_bytes >= 256 + static_cast<size_t>(T) * E * sizeof(float))
+    a.scratch_logits = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 256);
   return cuda_status(launch_router(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

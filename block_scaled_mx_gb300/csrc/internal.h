@@ -105,6 +105,8 @@ struct RouterArgs {
   float* topk_w;         // [T, k]
   int* status;
   uint64_t wait_limit_ns;
+  unsigned* counter;        // a word of the workspace: blocks finished (small batches; zero between calls)
+  float* scratch_logits;    // [T, E] in the workspace when the caller keeps no logits, or null
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 

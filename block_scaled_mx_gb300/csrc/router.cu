@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 
@@ -272,6 +273,216 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ small batches
+// For a few tokens the router is a matrix-vector product bound by streaming
+// the router weights: a block per 2 experts walks H in 256-element chunks,
+// four warps per expert, each taking a quarter of every chunk.  The block
+// stages each chunk of x (32 tokens x 512 bytes, rows padded by 16 bytes so
+// that a quarter-warp's 16-byte loads of 8 rows hit 32 distinct banks; up to
+// four such token tiles) and of its experts' rows in shared memory with
+// cp.async, three chunks in flight.  Lane t accumulates the dot products of
+// tokens t, t + 32, ... over its quarters in fp32 (8 exact products per
+// 16-byte step, two interleaved partial sums, the expert's weights a
+// broadcast shared-memory read); the four quarters' sums are added in a fixed
+// order.  The block that finishes last (a counter it resets; nobody
+// waits) selects every token's top-k from the logits in global memory, one
+// warp per token.
+constexpr int kRSmallMaxT = 128;
+constexpr int kRSmallExpertsPerBlock = 2;
+constexpr int kRSmallWarpsPerExpert = 4;
+constexpr int kRSmallRowWords = 132;  // 512 bytes of x + 16 bytes of padding, in 32-bit words
+
+struct RouterSmallParams {
+  const uint4* x;        // bf16 [T, H] as 16-byte groups
+  const uint4* w;        // bf16 [E, H]
+  const float* bias;
+  int T, H, E, k;
+  float* logits;         // [T, E] (the caller's, or the workspace's)
+  int32_t* ids;          // [T, k] or null
+  float* topk_w;
+  unsigned* done;        // blocks finished (zero between calls: the last block resets it)
+};
+
+// 8 products of bf16 pairs (exact in fp32) added to acc in element order.
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
+  const uint32_t x[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc = fmaf(__uint_as_float(x[i] << 16), __uint_as_float(w[i] << 16), acc);
+    acc = fmaf(__uint_as_float(x[i] & 0xFFFF0000u), __uint_as_float(w[i] & 0xFFFF0000u), acc);
+  }
+  return acc;
+}
+
+// One token's top-k by score = logit + bias (fp32 addition), lowest index on
+// equal scores, descending; weights: softmax of the chosen unbiased logits.
+// Lane l holds experts l, l + 32, ...
+template <int PER>
+__device__ __forceinline__ void router_select(const RouterSmallParams& p, int t, int lane) {
+  const int E = p.E, k = p.k;
+  const float* row = p.logits + static_cast<size_t>(t) * E;
+  float sc[PER], lg[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    lg[i] = e < E ? __ldcg(&row[e]) : 0.0f;
+    sc[i] = e < E ? lg[i] + (p.bias ? __ldg(&p.bias[e]) : 0.0f) : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float my_l = 0.0f;
+  int my_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bs = -INFINITY, bl = 0.0f;
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && (sc[i] > bs || bi == INT_MAX)) {
+        bs = sc[i];
+        bl = lg[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, off);
+      const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (os > bs || (os == bs && oi < bi)) {
+        bs = os;
+        bl = ol;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) {
+      my_l = bl;
+      my_i = bi;
+    }
+  }
+  float vmax = lane < k ? my_l : -INFINITY;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+  const float ex = lane < k ? expf(my_l - vmax) : 0.0f;
+  float sum = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (lane < k) {
+    p.ids[static_cast<size_t>(t) * k + lane] = my_i;
+    p.topk_w[static_cast<size_t>(t) * k + lane] = ex / sum;
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kRSmallStages = 3;                                   // chunks in flight
+constexpr int kRSmallXU4 = 32 * kRSmallRowWords / 4;               // one token tile's x rows, 16-byte units
+constexpr int kRSmallTiles = kRSmallMaxT / 32;                     // token tiles one sweep of H carries
+// one stage: nt token tiles of x rows, then the block's experts' chunks
+__host__ __device__ constexpr int rsmall_stage_u4(int nt) { return nt * kRSmallXU4 + kRSmallExpertsPerBlock * 32; }
+__host__ __device__ constexpr size_t rsmall_smem(int nt) {
+  return static_cast<size_t>(kRSmallStages) * rsmall_stage_u4(nt) * 16;
+}
+
+template <int PER>
+__global__ void __launch_bounds__(256) k_router_small(const RouterSmallParams p) {
+  extern __shared__ uint4 rsm[];  // kRSmallStages stages
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ew = warp / kRSmallWarpsPerExpert, wq = warp % kRSmallWarpsPerExpert;  // expert of the block, quarter
+  const int e = blockIdx.x * kRSmallExpertsPerBlock + ew;
+  __shared__ float part[8][32];
+  const int T = p.T, H8 = p.H / 8, nch = (H8 + 31) / 32;  // 16-byte groups per row, 256-element chunks
+  const int nt = (T + 31) / 32;                          // token tiles (all in one sweep of H)
+  const int stage_u4 = rsmall_stage_u4(nt);
+  // chunk c into stage c % S: thread i copies groups i, i + 256, ... of each
+  // [32 rows][32 groups] x tile, and threads i < 64 group i % 32 of the
+  // block's expert i / 32 (zero-filled past T or H); one commit group per
+  // chunk, empty ones past the last so that the wait count stays fixed
+  auto issue = [&](int c) {
+    if (c < nch) {
+      uint4* const sd = rsm + (c % kRSmallStages) * stage_u4;
+      for (int tt = 0; tt < nt; ++tt) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int i = tid + 256 * r, row = i >> 5, g = c * 32 + (i & 31), t = 32 * tt + row;
+          const bool ok = t < T && g < H8;
+          cp_async16(smem_u32(sd + tt * kRSmallXU4 + row * (kRSmallRowWords / 4) + (i & 31)),
+                     ok ? static_cast<const void*>(&p.x[static_cast<size_t>(t) * H8 + g]) : p.x, ok);
+        }
+      }
+      if (tid < kRSmallExpertsPerBlock * 32) {
+        const int ee = min(blockIdx.x * kRSmallExpertsPerBlock + (tid >> 5), p.E - 1);
+        const uint4* const wr = p.w + static_cast<size_t>(ee) * H8;
+        const bool okw = c * 32 + lane < H8;
+        cp_async16(smem_u32(sd + nt * kRSmallXU4 + tid), okw ? &wr[c * 32 + lane] : wr, okw);
+      }
+    }
+    cp_async_commit();
+  };
+  float acc0[kRSmallTiles], acc1[kRSmallTiles];
+#pragma unroll
+  for (int tt = 0; tt < kRSmallTiles; ++tt) acc0[tt] = acc1[tt] = 0.0f;
+#pragma unroll
+  for (int c = 0; c < kRSmallStages - 1; ++c) issue(c);
+  const int j0 = wq * (32 / kRSmallWarpsPerExpert);
+  for (int c = 0; c < nch; ++c) {
+    issue(c + kRSmallStages - 1);
+    cp_async_wait<kRSmallStages - 1>();
+    __syncthreads();
+    const uint4* const st = rsm + (c % kRSmallStages) * stage_u4;
+    const uint4* const wr = st + nt * kRSmallXU4 + ew * 32 + j0;
+#pragma unroll
+    for (int tt = 0; tt < kRSmallTiles; ++tt) {
+      if (tt < nt) {
+        const uint4* xr = st + tt * kRSmallXU4 + lane * (kRSmallRowWords / 4) + j0;
+#pragma unroll
+        for (int j = 0; j < 32 / kRSmallWarpsPerExpert; j += 2) {  // groups past H are zero in both
+          acc0[tt] = dot8_bf16(xr[j], wr[j], acc0[tt]);
+          acc1[tt] = dot8_bf16(xr[j + 1], wr[j + 1], acc1[tt]);
+        }
+      }
+    }
+    __syncthreads();  // the stage is refilled by the next iteration's copies
+  }
+  cp_async_wait<0>();
+#pragma unroll
+  for (int tt = 0; tt < kRSmallTiles; ++tt) {
+    if (tt < nt) {
+      part[warp][lane] = acc0[tt] + acc1[tt];
+      __syncthreads();
+      const int t = 32 * tt + lane;
+      if (wq == 0 && e < p.E && t < T) {
+        float v = part[warp][lane];
+#pragma unroll
+        for (int qq = 1; qq < kRSmallWarpsPerExpert; ++qq) v += part[warp + qq][lane];
+        p.logits[static_cast<size_t>(t) * p.E + e] = v;
+      }
+      __syncthreads();
+    }
+  }
+  if (!p.ids) return;
+  // the last block to finish selects (its reads of the other blocks' logits
+  // follow their fences and the counter)
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(p.done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (tid == 0) *p.done = 0u;  // ready for the next call
+  for (int t = warp; t < T; t += blockDim.x >> 5) router_select<PER>(p, t, lane);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 router_encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -288,9 +499,42 @@ PFN_cuTensorMapEncodeTiled_v12000 router_encode_fn() {
 }  // namespace
 
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  // a few tokens with somewhere to keep the logits: the small-batch kernel
+  float* small_logits = a.logits ? a.logits : a.scratch_logits;
+  if (a.T <= kRSmallMaxT && small_logits && a.H % 8 == 0) {
+    RouterSmallParams q{};
+    q.x = static_cast<const uint4*>(a.x);
+    q.w = static_cast<const uint4*>(a.w);
+    q.bias = a.bias;
+    q.T = a.T;
+    q.H = a.H;
+    q.E = a.E;
+    q.k = a.k;
+    q.logits = small_logits;
+    q.ids = a.ids;
+    q.topk_w = a.topk_w;
+    q.done = a.counter;
+    const unsigned grid = static_cast<unsigned>((a.E + kRSmallExpertsPerBlock - 1) / kRSmallExpertsPerBlock);
+    void (*kern)(RouterSmallParams) = a.E <= 32 ? k_router_small<1> : a.E <= 128 ? k_router_small<4> : k_router_small<16>;
+    // the shared-memory opt-in, once per device and kernel
+    {
+      static std::atomic<unsigned> allowed[kRMaxDevices];
+      int dev = 0;
+      cudaGetDevice(&dev);
+      const unsigned bit = a.E <= 32 ? 1u : a.E <= 128 ? 2u : 4u;
+      if (dev < 0 || dev >= kRMaxDevices || !(allowed[dev].load(std::memory_order_relaxed) & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(rsmall_smem(kRSmallTiles)));
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kRMaxDevices) allowed[dev].fetch_or(bit, std::memory_order_relaxed);
+      }
+    }
+    kern<<<grid, 256, rsmall_smem((a.T + 31) / 32), stream>>>(q);
+    return cudaGetLastError();
+  }
   auto encode = router_encode_fn();
   if (!encode) return cudaErrorNotSupported;
-  if (a.T == 0) return cudaSuccess;
   RouterParams p{};
   p.T = a.T;
   p.H = a.H;

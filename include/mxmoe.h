@@ -120,8 +120,8 @@ MX_API int moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
                    mx_stream_t stream);
 
 /* Router GEMM with top-k in its epilogue (the step ahead of moe_route_topk):
- *   logits[t, e] = sum_h x[t, h] * w_router[e, h]   (bf16 inputs, fp32 accumulation
- *     on the tensor cores; products of bf16 values are exact in fp32)
+ *   logits[t, e] = sum_h x[t, h] * w_router[e, h]   (bf16 inputs, fp32 accumulation;
+ *     products of bf16 values are exact in fp32)
  *   topk_ids[t, :] = the k experts with the largest score logit + bias[e]
  *     (one fp32 addition), lowest index on ties, descending score order
  *   topk_w[t, :] = softmax of the chosen experts' unbiased logits (fp32).
@@ -131,7 +131,14 @@ MX_API int moe_route_topk(const float* logits, int T, int E, int k, int32_t* top
  *     pages give no router).  logits [T, E] or NULL.  topk_ids and topk_w
  *     both NULL: logits only (then logits must be given).
  *   ws: a 256-byte-aligned workspace of at least 256 bytes, zero-filled once;
- *     its first word is the status word moe_get_status reads.
+ *     its first word is the status word moe_get_status reads, its second a
+ *     counter of the small-batch kernel.
+ * Up to 128 tokens with somewhere to keep the logits (logits given, or ws of
+ * at least 256 + 4*T*E bytes) run a CUDA-core kernel over blocks of 2 experts
+ * (the router is then a weight-streaming matrix-vector product) whose last
+ * block selects; larger batches run the tensor-core GEMM with the selection
+ * in its epilogue.  Both sum the same exact bf16 products in fp32 (in
+ * different orders).
  * Errors: MX_ERR_INVALID_ARG, MX_ERR_UNSUPPORTED (H % 64, E > 512, k > 16),
  * MX_ERR_ALIGNMENT, MX_ERR_WORKSPACE.
  * Source: the MI355X page, Figure 4 and its passage (tokens are routed to

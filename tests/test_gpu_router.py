@@ -91,3 +91,33 @@ def test_router_logits_only_and_ties(T, H, E, k):
     assert np.array_equal(ids.cpu().numpy(), rid)
     np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
     assert mx.moe_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("T,H,E,k", [(32, 4096, 128, 8), (6, 2048, 512, 8), (64, 320, 40, 5), (1, 64, 8, 1),
+                                     (128, 4096, 128, 8), (97, 192, 300, 16)])
+def test_router_small_batch_without_caller_logits(T, H, E, k):
+    """Up to 128 tokens the logits may live in a larger workspace instead of a
+    caller buffer (the small-batch kernel); the selection matches the run that
+    returns its logits, and both match the oracle's selection on those logits."""
+    x, w, bias = _inputs(T, H, E, 7 * T + E, 0.5)
+    xd, wd, bd = x.cuda(), w.cuda(), bias.cuda()
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    ids = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    ws = mx.alloc_workspace(256)
+    mx.moe_route_gemm_topk(xd, wd, k, ws, bias=bd, logits=logits, topk_ids=ids, topk_w=tw)
+    big = mx.alloc_workspace(256 + 4 * T * E)
+    ids2 = torch.empty_like(ids)
+    tw2 = torch.empty_like(tw)
+    for _ in range(2):  # the block counter is ready again after a call
+        mx.moe_route_gemm_topk(xd, wd, k, big, bias=bd, topk_ids=ids2, topk_w=tw2)
+        assert torch.equal(ids2, ids)
+        assert torch.equal(tw2, tw)
+    assert mx.moe_get_status(ws) == 0 and mx.moe_get_status(big) == 0
+    got = logits.cpu().numpy()
+    ref = oracle.router_logits(_bits(x), _bits(w))
+    absum = np.abs(x.double().numpy()) @ np.abs(w.double().numpy()).T
+    assert np.all(np.abs(got - ref) <= H * 2.0 ** -24 * absum + 1e-30)
+    rid, rw = oracle.route_topk_biased(got, bias.numpy(), k)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_allclose(tw.cpu().numpy(), rw, rtol=2e-6, atol=1e-7)
