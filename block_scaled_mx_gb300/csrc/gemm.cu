@@ -261,7 +261,11 @@ __device__ __forceinline__ void issue_chunk_a4(uint32_t d0, uint32_t d1, uint32_
 // launches share one kernel (-1): the down launch's CTAs start as the gate/up
 // CTAs leave, and with the gate/up launch's code still in the caches; with a
 // kernel of its own the 16-token layer was 7 us slower (its code fetched cold).
-template <bool PAIR, bool BT, int EPI>
+// A4: MXFP4 activations (packed E2M1 operands, kind::mxf4): 1 yes, 0 no, -1
+// either (p.a4).  The narrow schedule's kernels are specialised (the common
+// MXFP8-activation kernel leaves the packed-FP4 code out: less code to fetch
+// cold at the start of a small layer).
+template <bool PAIR, bool BT, int EPI, int A4 = -1>
 __global__ void __launch_bounds__(kThreads, 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
@@ -418,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const uint32_t b_row = p.b_row;
-      const int kx = p.a4 ? 64 : 128;  // bytes of a K chunk in a token row
+      const int kx = (A4 < 0 ? p.a4 != 0 : A4 == 1) ? 64 : 128;  // bytes of a K chunk in a token row
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 4u * b_row : static_cast<uint32_t>(p.brows) * b_row;
       const uint32_t bytes = ((PAIR || p.one ? 1u : 2u) * p.a_tx + b_bytes) * static_cast<uint32_t>(kps);
       for (int ks = 0; ks < NK; ks += kps) {
@@ -510,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_base = smem_u32(base + p.off_b);
       const uint32_t b_stride16 = (static_cast<uint32_t>(p.brows) * p.b_row) >> 4;
       const uint32_t a16 = p.a_slot >> 4;  // A chunk slot stride in 16-byte units
-      const bool a4 = p.a4 != 0;
+      const bool a4 = A4 < 0 ? p.a4 != 0 : A4 == 1;
       const uint32_t kps = static_cast<uint32_t>(p.kps);
       // descriptors of slot 0 (start address field is addr >> 4; slots add to it)
       const uint32_t a_lo0 = desc_lo_sw128(a_base);
@@ -765,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* const h_scales = p.h_scales;
         const bool act_oai = p.act != 0;
         const float alpha = p.alpha, limit = p.limit;
-        const bool h4 = p.a4 != 0;  // h re-quantised to MXFP4 (packed E2M1, I/2 bytes a row)
+        const bool h4 = A4 < 0 ? p.a4 != 0 : A4 == 1;  // h re-quantised to MXFP4 (packed E2M1, I/2 bytes a row)
         // 8 columns at a time, each step over all 8 so that the per-column
         // chains (SwiGLU, warp amax, exponent, encode) overlap; the tensor-
         // memory loads of the warp's next 8 columns are in flight while the
@@ -1293,15 +1297,15 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const bool bt = a.b_scales_t != nullptr;
   const bool narrow = a.bn <= 64 && !pair && !bt;
   void (*kernel)(GemmParams, CUtensorMap, CUtensorMap) =
-      narrow ? k_grouped_gemm<false, false, -1>
+      narrow ? (a.a4 ? k_grouped_gemm<false, false, -1, 1> : k_grouped_gemm<false, false, -1, 0>)
       : a.epi == 0 ? (pair ? (bt ? k_grouped_gemm<true, true, 0> : k_grouped_gemm<true, false, 0>)
                            : (bt ? k_grouped_gemm<false, true, 0> : k_grouped_gemm<false, false, 0>))
                    : (pair ? k_grouped_gemm<true, false, 1> : k_grouped_gemm<false, false, 1>);
   // the shared-memory opt-in is per device and kernel and only ever raised:
   // skip the driver call when a launch on this device already allowed this much
   {
-    static std::atomic<int> smem_allowed[7][kMaxDevices];
-    const int which = narrow ? 6 : a.epi == 0 ? (pair ? 2 : 0) + (bt ? 1 : 0) : 4 + (pair ? 1 : 0);
+    static std::atomic<int> smem_allowed[8][kMaxDevices];
+    const int which = narrow ? 6 + (a.a4 ? 1 : 0) : a.epi == 0 ? (pair ? 2 : 0) + (bt ? 1 : 0) : 4 + (pair ? 1 : 0);
     std::atomic<int>* allowed = (dev >= 0 && dev < kMaxDevices) ? &smem_allowed[which][dev] : nullptr;
     if (!allowed || allowed->load(std::memory_order_relaxed) < static_cast<int>(smem)) {
       cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
