@@ -497,7 +497,9 @@ cudaError_t launch_permute(const int32_t* ids, int T, int E, int k, int32_t* cou
 // computes the whole permutation, which needs T <= kPermuteChunk.  It lets the
 // next grid (the gate/up GEMM, launched programmatically dependent) start its
 // set-up at once.
-template <int PER, bool PERMUTE>
+// E2M1: quantise to MXFP4 (one instantiation per activation format: the
+// first launch of a layer runs its code cold).
+template <int PER, bool PERMUTE, bool E2M1>
 __global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
   extern __shared__ uint32_t bits[];
   __shared__ int s_last;
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kPermuteChunk) k_prologue(PrologueArgs a) {
     topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
-  if (a.act_e2m1)
+  if (E2M1)
     for (int64_t i = first; i - lane < a.n8; i += stride)
       quantize_act_step_e2m1(a.x, a.n8, i, lane, reinterpret_cast<uint32_t*>(a.codes), a.scales);
   else
@@ -537,12 +539,21 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
   const size_t smem = a.permute ? permute_block_smem(a.T, a.E, a.k) : 0;
   const unsigned g = static_cast<unsigned>(blocks);
   void (*kern)(PrologueArgs);
-  if (a.permute)
-    kern = a.E <= 32 ? k_prologue<1, true> : a.E <= 128 ? k_prologue<4, true>
-         : a.E <= 512 ? k_prologue<16, true> : k_prologue<32, true>;
-  else
-    kern = a.E <= 32 ? k_prologue<1, false> : a.E <= 128 ? k_prologue<4, false>
-         : a.E <= 512 ? k_prologue<16, false> : k_prologue<32, false>;
+  if (a.act_e2m1) {
+    if (a.permute)
+      kern = a.E <= 32 ? k_prologue<1, true, true> : a.E <= 128 ? k_prologue<4, true, true>
+           : a.E <= 512 ? k_prologue<16, true, true> : k_prologue<32, true, true>;
+    else
+      kern = a.E <= 32 ? k_prologue<1, false, true> : a.E <= 128 ? k_prologue<4, false, true>
+           : a.E <= 512 ? k_prologue<16, false, true> : k_prologue<32, false, true>;
+  } else {
+    if (a.permute)
+      kern = a.E <= 32 ? k_prologue<1, true, false> : a.E <= 128 ? k_prologue<4, true, false>
+           : a.E <= 512 ? k_prologue<16, true, false> : k_prologue<32, true, false>;
+    else
+      kern = a.E <= 32 ? k_prologue<1, false, false> : a.E <= 128 ? k_prologue<4, false, false>
+           : a.E <= 512 ? k_prologue<16, false, false> : k_prologue<32, false, false>;
+  }
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
