@@ -566,11 +566,12 @@ cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {
 // The first launch of the layer for T > kPermuteChunk: one grid whose blocks
 // are all resident at once (its size comes from the occupancy query) runs, with
 // a grid barrier (a global counter, bounded waits) between the phases:
-//   0. routing (warp per token), quantisation of x, zeroing of out;
+//   0. routing (warp per token);
 //   1. the chunked permutation's first pass, one block per chunk of 256
 //      tokens, the last of them (counter, nobody waits) turning the per-chunk
-//      counts into the expert offsets and chunk bases;
-//   2. the scatter of every slot to its position;
+//      counts into the expert offsets and chunk bases; the other blocks
+//      quantise x meanwhile;
+//   2. the scatter of every slot to its position; the other blocks zero out;
 //   3. (wide schedule) the copy of each slot's activation row into slot
 //      order, the B operand the wide gate/up GEMM loads as 2-D boxes, and of
 //      its scales into K-chunk-major order.
@@ -635,24 +636,43 @@ __global__ void __launch_bounds__(kPermuteChunk) k_prologue_big(PrologueArgs a, 
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned G = gridDim.x;
-  // phase 0
-  for (int t = blockIdx.x * (kPermuteChunk / 32) + warp; t < a.T; t += gridDim.x * (kPermuteChunk / 32))
-    topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
+  const int nchunks = (a.T + kPermuteChunk - 1) / kPermuteChunk;
+  // the streaming work (quantisation of x, zeroing of out) runs on the blocks
+  // the permutation leaves idle (blocks >= nchunks) during its two phases,
+  // or in phase 0 when there are none
+  const bool spare = static_cast<int>(G) > nchunks;
+  auto quantize = [&](int64_t first, int64_t stride) {
+    if (a.act_e2m1)
+      for (int64_t i = first; i - lane < a.n8; i += stride)
+        quantize_act_step_e2m1(a.x, a.n8, i, lane, reinterpret_cast<uint32_t*>(a.codes), a.scales);
+    else
+      for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
+  };
+  auto zero_out = [&](int64_t first, int64_t stride) {
+    for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  };
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t first = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid;
-  if (a.act_e2m1)
-    for (int64_t i = first; i - lane < a.n8; i += stride)
-      quantize_act_step_e2m1(a.x, a.n8, i, lane, reinterpret_cast<uint32_t*>(a.codes), a.scales);
-  else
-    for (int64_t i = first; i - lane < a.n8; i += stride) quantize_act_step(a.x, a.n8, i, lane, a.codes, a.scales);
-  for (int64_t i = first; i < a.n_out4; i += stride) a.out[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int64_t spare_stride = static_cast<int64_t>(static_cast<int>(G) - nchunks) * blockDim.x;
+  const int64_t spare_first = static_cast<int64_t>(static_cast<int>(blockIdx.x) - nchunks) * blockDim.x + tid;
+  // phase 0: routing
+  for (int t = blockIdx.x * (kPermuteChunk / 32) + warp; t < a.T; t += gridDim.x * (kPermuteChunk / 32))
+    topk_token<PER>(a.logits, t, a.E, a.k, lane, a.ids, a.topk_w);
+  if (!spare) {
+    quantize(first, stride);
+    zero_out(first, stride);
+  }
   if (!grid_barrier(b.bar, G, a.sc.status, b.wait_limit_ns)) return;
-  // phase 1: counting pass, offsets and chunk bases (last chunk block)
-  const int nchunks = (a.T + kPermuteChunk - 1) / kPermuteChunk;
+  // phase 1: counting pass, offsets and chunk bases (last chunk block); the
+  // spare blocks quantise x
   if (static_cast<int>(blockIdx.x) < nchunks)
     permute_count_block(a.ids, a.T, a.E, a.k, a.counts, a.offsets, a.sorted_slot, a.sc, nchunks, blockIdx.x, bits);
+  else
+    quantize(spare_first, spare_stride);
   if (!grid_barrier(b.bar, 2 * G, a.sc.status, b.wait_limit_ns)) return;
-  // phase 2: scatter (as k_permute_scatter; the counters are reset for the next call)
+  // phase 2: scatter (as k_permute_scatter; the counters are reset for the
+  // next call); the spare blocks zero out
+  if (static_cast<int>(blockIdx.x) >= nchunks) zero_out(spare_first, spare_stride);
   if (static_cast<int>(blockIdx.x) < nchunks) {
     const int chunk = blockIdx.x;
     const int t = chunk * kPermuteChunk + tid;
