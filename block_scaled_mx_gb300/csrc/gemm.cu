@@ -18,7 +18,7 @@
 // stage is full once its TMA bytes have landed and the scale-staging warps
 // have put its scale factors into tensor memory.
 //
-// Warp roles (448 threads):
+// Warp roles (448 threads; 576 for the wide gate/up kernel):
 //   warp 0      TMA producer: weight blocks (tensor map, 128B swizzle, MXFP4
 //               unpacked to the 16-byte-aligned form by the TMA) and token
 //               rows (tensor map)
@@ -29,9 +29,9 @@
 //               every stage, from global memory into every TMEM lane quarter
 //               with tcgen05.st
 //   warps 6-13  epilogue: tcgen05.ld of the fp32 accumulators, SwiGLU +
-//               MXFP8 re-quantisation or weighted combine; warps w and w + 4
-//               share a TMEM lane quarter (w mod 4) and take alternate column
-//               chunks
+//               MXFP8 re-quantisation or weighted combine; warps w, w + 4
+//               (and w + 8: warps 6-17 in the wide gate/up kernel) share a TMEM
+//               lane quarter (w mod 4) and take its column chunks in turn
 // Every wait is bounded (wall clock); a wait that runs out sets
 // MX_ERR_TIMEOUT in the status word and every role unwinds.
 #include <cuda.h>
@@ -48,12 +48,10 @@
 
 namespace mxk {
 
-constexpr int kThreads = 448;
 constexpr int kWarpTma = 0;
 constexpr int kWarpMma = 1;     // with a CTA pair, rank 1's warp relays stage completions
 constexpr int kWarpSf0 = 2;     // warps 2..5: TMEM lane quarters 2, 3, 0, 1
-constexpr int kWarpEpi0 = 6;    // warps 6..13: two per lane quarter
-constexpr int kEpiWarps = 8;
+constexpr int kWarpEpi0 = 6;    // warps 6..13 (6..17): two (three) per lane quarter
 // per epilogue warp, a transpose tile: 16 columns of E4M3 codes (gate/up) or
 // 8 columns of fp32 (down)
 __host__ __device__ constexpr uint32_t epi_buf_bytes(int epi) { return epi == 0 ? 512u : 1024u; }
@@ -265,10 +263,21 @@ __device__ __forceinline__ void issue_chunk_a4(uint32_t d0, uint32_t d1, uint32_
 // either (p.a4).  The narrow schedule's kernels are specialised (the common
 // MXFP8-activation kernel leaves the packed-FP4 code out: less code to fetch
 // cold at the start of a small layer).
+// The wide gate/up kernel (single CTA, gathered rows) runs 12 epilogue warps
+// (three per lane quarter): its SwiGLU/requantisation epilogue drains the one
+// accumulator buffer while the next tile's MMAs wait.
+__host__ __device__ constexpr int epi_warps(bool pair, bool bt, int epi) { return (!pair && bt && epi == 0) ? 12 : 8; }
+__host__ __device__ constexpr int gemm_threads(bool pair, bool bt, int epi) {
+  return (kWarpEpi0 + epi_warps(pair, bt, epi)) * 32;
+}
+
 template <bool PAIR, bool BT, int EPI, int A4 = -1>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(PAIR, BT, EPI), 1)
     k_grouped_gemm(const __grid_constant__ GemmParams p, const __grid_constant__ CUtensorMap tm_a,
                    const __grid_constant__ CUtensorMap tm_b) {
+  constexpr int kEW = epi_warps(PAIR, BT, EPI);        // epilogue warps
+  constexpr int kTh = gemm_threads(PAIR, BT, EPI);     // threads
+  constexpr int kNH = kEW / 4;                         // epilogue warps per lane quarter
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -316,12 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sh.acc_full[a]), 1);
-      mbar_init(smem_u32(&sh.acc_empty[a]), PAIR ? 2 * kEpiWarps : kEpiWarps);
+      mbar_init(smem_u32(&sh.acc_empty[a]), PAIR ? 2 * kEW : kEW);
     }
     mbar_init(smem_u32(sh.drain), 1);
     mbar_init(smem_u32(sh.exit_bar), 1);
-    mbar_init(smem_u32(sh.xfull), kEpiWarps);
-    mbar_init(smem_u32(sh.xfree), kEpiWarps);
+    mbar_init(smem_u32(sh.xfull), kEW);
+    mbar_init(smem_u32(sh.xfree), kEW);
     for (int s = 0; s < S; ++s) sh.sf_cnt[s] = 0u;
     *sh.abort_flag = 0;
     fence_mbar_init();
@@ -341,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   // tile prefix: each thread owns a run of experts, warp 0..11 shuffle-scan
   {
-    __shared__ int warp_tot[kThreads / 32];
-    const int per = (E1 + kThreads - 1) / kThreads;
+    __shared__ int warp_tot[kTh / 32];
+    const int per = (E1 + kTh - 1) / kTh;
     const int b0 = min(tid * per, E1), b1 = min(b0 + per, E1);
     int run = 0;
     for (int e = b0; e < b1; ++e) {
@@ -739,10 +748,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEpiWarps) {
+  } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + kEW) {
     // ================================================================ epilogue
     const int q = warp & 3;                   // TMEM lane quarter of this warp
-    const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks
+    const int half = (warp - kWarpEpi0) >> 2;  // which alternate column chunks (of kNH)
     uint8_t* const ebuf =
         base + p.off_epi + static_cast<uint32_t>(warp - kWarpEpi0) * epi_buf_bytes(EPI < 0 ? p.epi : EPI);
     const uint32_t acc_bufs = static_cast<uint32_t>(p.acc_bufs);
@@ -890,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           xph ^= 1u;
         } else {
         uint32_t ga[8], ua[8], gb[8], ub[8];
-        int c0 = 8 * half;
+        int c0 = 8 * half;  // 8-column chunks dealt round-robin to the quarter's kNH warps
         if (c0 < tl.rows) {
           __syncwarp();
           tmem_ld_32x32b_x8(d0 + c0, ga);
@@ -898,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait();
         }
         while (c0 < tl.rows) {
-          const int c1 = c0 + 16;
+          const int c1 = c0 + 8 * kNH;
           if (c1 < tl.rows) {
             tmem_ld_32x32b_x8(d0 + c1, gb);
             tmem_ld_32x32b_x8(d1 + c1, ub);
@@ -906,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           process(ga, ua, c0);
           if (c1 >= tl.rows) break;
           tmem_ld_wait();
-          const int c2 = c1 + 16;
+          const int c2 = c1 + 8 * kNH;
           if (c2 < tl.rows) {
             tmem_ld_32x32b_x8(d0 + c2, ga);
             tmem_ld_32x32b_x8(d1 + c2, ua);
@@ -924,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* const out = p.out;
         const int H = p.H;
         float* const ebf = reinterpret_cast<float*>(ebuf);
-        for (int c0 = 32 * half; c0 < tl.rows; c0 += 64) {
+        for (int c0 = 32 * half; c0 < tl.rows; c0 += 32 * kNH) {
           // lane n: token and combine weight of column c0 + n
           int tok = 0;
           float wt = 0.0f;
@@ -1187,7 +1196,8 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   int max_smem = 0;
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const uint32_t epi_bytes = kEpiWarps * epi_buf_bytes(a.epi);
+  const int n_epi_warps = epi_warps(pair, a.b_scales_t != nullptr, a.epi);
+  const uint32_t epi_bytes = static_cast<uint32_t>(n_epi_warps) * epi_buf_bytes(a.epi);
   // a pair's gate/up epilogue receives the partner's half of the tokens here
   const uint32_t x_bytes = (pair && a.epi == 0) ? 128u * p.xs * 4u : 0u;
   const uint32_t fixed =
@@ -1321,14 +1331,14 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t stream) {
   const int grid = units * (pair ? 2 : 1);
   const int timed = timer_begin(a.epi, stream);
   if (!a.pdl && !pair) {
-    kernel<<<grid, kThreads, smem, stream>>>(p, tm_a, tm_b);
+    kernel<<<grid, gemm_threads(pair, bt, a.epi), smem, stream>>>(p, tm_a, tm_b);
     const cudaError_t e = cudaGetLastError();
     timer_end(timed, stream);
     return e;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(gemm_threads(pair, bt, a.epi));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
