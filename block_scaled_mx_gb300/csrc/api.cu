@@ -23,11 +23,14 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MX_OK : MX_ERR_CUDA; 
 // expert (known on the host, no device read).  The narrow decode schedule
 // (16 or 32 rows) streams weights with two accumulator buffers; 16-row tiles
 // (a few rows per expert) free shared memory for a third pipeline stage at the
-// price of a second tile for experts with more rows (the shared expert).  The wide prefill
-// schedule reuses each weight tile over many token rows; for the gate/up GEMM
-// 192 with one accumulator buffer: a block-scaled MMA costs about the same issue
-// time for any N up to 192, so doubling N over 96 (the widest tile with two
-// buffers) outweighs the epilogue no longer overlapping the MMAs.
+// price of a second tile for experts with more rows (the shared expert).  The
+// wide prefill schedule reuses each weight tile over many token rows, and an
+// SM's operand intake is its limit there, so the tile is as wide as tensor
+// memory allows with three pipeline stages of scale factors: 208 rows.  The
+// gate/up GEMM then holds one accumulator buffer (2 x 208 columns of g and u),
+// the down GEMM two (one W2 row block a tile, M = 128: the atomic-combine
+// epilogue overlaps the next tile's MMAs).  On the 8192-token layer 208 beat
+// 192 by 4% in each GEMM; 224 leaves room for only two stages and lost.
 // `which`: 0 gate/up, 1 down.
 int choose_bn(int T, int E, int k, int which) {
   const char* env = std::getenv(which == 1 && std::getenv("MXMOE_BN2") ? "MXMOE_BN2" : "MXMOE_BN");
@@ -38,12 +41,7 @@ int choose_bn(int T, int E, int k, int which) {
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
   if (mean_rows < 12.0) return 16;  // smaller B tiles leave room for a third stage
   if (mean_rows < 48.0) return 32;
-  // down GEMM: 192 rows with one W2 row block a tile (M = 128) keeps two
-  // accumulator buffers (the atomic-combine epilogue overlaps the next tile's
-  // MMAs) with MMAs of N = 192, past the per-instruction issue floor of
-  // narrower ones (the 8192-token layer: 0.67 ms against 0.71 ms for two row
-  // blocks and 96 rows)
-  return 192;
+  return 208;
 }
 
 int check_gemm_shape(int T, int H, int I, int E, int k, int fmt) {
