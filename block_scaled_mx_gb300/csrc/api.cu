@@ -39,7 +39,10 @@ int choose_bn(int T, int E, int k, int which) {
     if (v >= 16 && v <= 224 && v % 16 == 0) return v;
   }
   const double mean_rows = static_cast<double>(T) * (k + 1) / (E + 1);
-  if (mean_rows < 12.0) return 16;  // smaller B tiles leave room for a third stage
+  // gate/up: smaller B tiles leave room for a third stage; down: 32 rows (the
+  // shared expert's T rows in half the tiles, each reading the expert's W2
+  // once more: decode_mxfp4 layer 272 -> 267 us)
+  if (mean_rows < 12.0) return which == 1 ? 32 : 16;
   if (mean_rows < 48.0) return 32;
   return 208;
 }
