@@ -418,18 +418,24 @@ __global__ void __launch_bounds__(gemm_threads(PAIR, BT, EPI), 1)
       const int b_row0 = tl.p0 + (PAIR ? static_cast<int>(sh.rank) * (n_mma >> 1) : 0);
       // the tile's two row blocks are prepared blocks 2m and 2m + 1 of each K
       // chunk (gate and up block m in W1): one TMA box
-      // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token)
+      // gather: lane g loads rows 4g..4g+3 (padding rows repeat the last token).
+      // The decode-size kernel reads their tokens once the tile's first weight
+      // copy is on its way; the wide kernels (no gather) keep the read here,
+      // out of their stage loop.
       const int n4 = gather ? (tl.rows + 3) / 4 : 0;
       int tok[4] = {0, 0, 0, 0};
-      if (gather && lane < n4) {
+      auto read_tok = [&]() {
+        if (gather && lane < n4) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = min(4 * lane + j, tl.rows - 1);
-          const int tt = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
-          if (tt < 0 || tt >= p.T) set_status(p.status, MX_ERR_DEVICE_ARG);
-          tok[j] = (tt < 0 || tt >= p.T) ? 0 : tt;
+          for (int j = 0; j < 4; ++j) {
+            const int r = min(4 * lane + j, tl.rows - 1);
+            const int tt = __ldg(&p.sorted_slot[tl.p0 + r]) / (p.k + 1);
+            if (tt < 0 || tt >= p.T) set_status(p.status, MX_ERR_DEVICE_ARG);
+            tok[j] = (tt < 0 || tt >= p.T) ? 0 : tt;
+          }
         }
-      }
+      };
+      if (EPI >= 0) read_tok();
       const uint32_t b_row = p.b_row;
       const int kx = (A4 < 0 ? p.a4 != 0 : A4 == 1) ? 64 : 128;  // bytes of a K chunk in a token row
       const uint32_t b_bytes = gather ? static_cast<uint32_t>(n4) * 4u * b_row : static_cast<uint32_t>(p.brows) * b_row;
@@ -452,6 +458,7 @@ __global__ void __launch_bounds__(gemm_threads(PAIR, BT, EPI), 1)
           uint8_t* a_s = base + p.off_a + su * p.a_slot;
           tma_load_4d(smem_u32(a_s), &tm_a, 0, 0, blk_row, (tl.e + p.e_base) * NK + ks, full);
         }
+        if (EPI < 0 && ks == 0) read_tok();
         if (!b_ready) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           b_ready = true;
@@ -634,6 +641,21 @@ __global__ void __launch_bounds__(gemm_threads(PAIR, BT, EPI), 1)
       // the tile's first prepared row block (a pair's CTA: its own, the only one)
       const int blk_row = p.one ? tl.m : 2 * tl.m + (PAIR ? static_cast<int>(sh.rank) : 0);
       const bool two = !PAIR && !p.one && 2 * tl.m + 1 < p.RB;
+      // warm L2 with the tile's weight-scale blocks (128-byte lines, 4 per
+      // block, one or two blocks per chunk): the per-stage loads below then hit
+      // L2 instead of waiting on DRAM.  Kernels that run the gate/up epilogue
+      // issue them before reading the tile's tokens from the permutation (a
+      // dependent load); the down-only kernel after its row offsets.
+      auto prefetch_wsc = [&]() {
+        const int lines = two ? 8 : 4;
+        const int sft = tid - kWarpSf0 * 32;
+        for (int i = sft; i < NK * lines; i += 128) {
+          const int kc = i / lines, line = i - kc * lines;
+          const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + blk_row) * 32;
+          prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
+        }
+      };
+      if (EPI != 1) prefetch_wsc();
       // rows 32j + lane of this tile: the word offset of their scale rows
       // (-1: a padding row)
       int roww[8];
@@ -655,18 +677,7 @@ __global__ void __launch_bounds__(gemm_threads(PAIR, BT, EPI), 1)
           roww[j] = src_row * (K32 / 4);
         }
       }
-      // warm L2 with the tile's weight-scale blocks (128-byte lines, 4 per
-      // block, one or two blocks per chunk): the per-stage loads below then hit
-      // L2 instead of waiting on DRAM
-      {
-        const int lines = two ? 8 : 4;
-        const int sft = tid - kWarpSf0 * 32;
-        for (int i = sft; i < NK * lines; i += 128) {
-          const int kc = i / lines, line = i - kc * lines;
-          const uint4* blk = wsc + static_cast<size_t>(((tl.e + p.e_base) * NK + kc) * p.RB + blk_row) * 32;
-          prefetch_l2(reinterpret_cast<const uint8_t*>(blk) + line * 128);
-        }
-      }
+      if (EPI == 1) prefetch_wsc();
       auto load = [&](ScaleBuf& b, int kc) {
         if (BT) {
           const uint32_t* const bk = bsc + static_cast<size_t>(kc) * static_cast<size_t>(p.n_rows);
