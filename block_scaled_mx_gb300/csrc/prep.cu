@@ -168,50 +168,55 @@ cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, ui
 }
 
 // ------------------------------------------------------------------ router top-k
-// One warp per token.  Lane l holds logits l, l+32, ... in registers; each of
-// the k rounds takes the warp-wide maximum (larger logit, then lower index)
-// among the logits not yet taken.  Lane j keeps round j's winner, so ids come
+// One warp per token.  Lane l holds logits l, l+32, ... in registers as
+// order-preserving 32-bit keys (sign-magnitude floats mapped onto unsigned
+// order; -0 folded into +0 first, so equal logits give equal keys).  Each of
+// the k rounds takes the warp-wide maximum key among the logits not yet taken
+// (one warp reduction), then the lowest expert index holding it (a second):
+// larger logit, then lower index.  Lane j keeps round j's winner, so ids come
 // out in descending-logit order; softmax over the k winners in fp32.
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t b = __float_as_uint(x + 0.0f);  // -0 -> +0
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
 template <int PER>
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int lane, int32_t* __restrict__ ids,
                                            float* __restrict__ wout) {
   const float* row = logits + static_cast<int64_t>(t) * E;
-  float v[PER];
+  uint32_t key[PER];  // 0: past E (below every logit's key, -inf's included)
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
-    v[i] = e < E ? __ldg(&row[e]) : -INFINITY;
+    key[i] = e < E ? order_key(__ldg(&row[e])) : 0u;
   }
   uint32_t taken = 0;
-  float my_v = -INFINITY;
+  uint32_t my_key = 0;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = INT_MAX;
+    // this lane's best untaken key; on equal keys the lower i (lower index)
+    uint32_t bk = 0;
+    int bl = 0;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (v[i] > bv || bi == INT_MAX)) {
-        bv = v[i];
-        bi = e;
+    for (int i = 0; i < PER; ++i)
+      if (!((taken >> i) & 1u) && key[i] > bk) {
+        bk = key[i];
+        bl = i;
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int bi = static_cast<int>(__reduce_min_sync(0xffffffffu, bk == m && m != 0u
+                                                                        ? static_cast<uint32_t>(lane + 32 * bl)
+                                                                        : 0xFFFFFFFFu));
+    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      my_v = bv;
+      my_key = m;
       my_i = bi;
     }
   }
+  const float my_v = key_value(my_key);
   const float vmax = __shfl_sync(0xffffffffu, my_v, 0);
   float ex = lane < k ? expf(my_v - vmax) : 0.0f;
   float sum = ex;
