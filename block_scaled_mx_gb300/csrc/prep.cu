@@ -11,6 +11,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "select.cuh"
 
 namespace mxk {
 
@@ -175,13 +176,6 @@ cudaError_t launch_quantize_weights(const float* w, int64_t n_elems, int fmt, ui
 // (one warp reduction), then the lowest expert index holding it (a second):
 // larger logit, then lower index.  Lane j keeps round j's winner, so ids come
 // out in descending-logit order; softmax over the k winners in fp32.
-__device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t b = __float_as_uint(x + 0.0f);  // -0 -> +0
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 template <int PER>
 __device__ __forceinline__ void topk_token(const float* __restrict__ logits, int t, int E, int k,
                                            int lane, int32_t* __restrict__ ids,

@@ -26,6 +26,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
+#include "select.cuh"
 
 namespace mxk {
 
@@ -317,47 +318,43 @@ __device__ __forceinline__ float dot8_bf16(uint4 a, uint4 b, float acc) {
 
 // One token's top-k by score = logit + bias (fp32 addition), lowest index on
 // equal scores, descending; weights: softmax of the chosen unbiased logits.
-// Lane l holds experts l, l + 32, ...
+// Lane l holds experts l, l + 32, ... as order-preserving score keys; each
+// round's winner is two warp reductions (the largest key, then the lowest
+// index holding it), its logit taken from the lane that holds it.
 template <int PER>
 __device__ __forceinline__ void router_select(const RouterSmallParams& p, int t, int lane) {
   const int E = p.E, k = p.k;
   const float* row = p.logits + static_cast<size_t>(t) * E;
-  float sc[PER], lg[PER];
+  float lg[PER];
+  uint32_t key[PER];  // 0: past E
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
     lg[i] = e < E ? __ldcg(&row[e]) : 0.0f;
-    sc[i] = e < E ? lg[i] + (p.bias ? __ldg(&p.bias[e]) : 0.0f) : -INFINITY;
+    key[i] = e < E ? order_key(lg[i] + (p.bias ? __ldg(&p.bias[e]) : 0.0f)) : 0u;
   }
   uint32_t taken = 0;
   float my_l = 0.0f;
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bs = -INFINITY, bl = 0.0f;
-    int bi = INT_MAX;
+    uint32_t bk = 0;
+    float bl = 0.0f;
+    int bs = 0;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && (sc[i] > bs || bi == INT_MAX)) {
-        bs = sc[i];
+    for (int i = 0; i < PER; ++i)
+      if (!((taken >> i) & 1u) && key[i] > bk) {
+        bk = key[i];
         bl = lg[i];
-        bi = e;
+        bs = i;
       }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float os = __shfl_xor_sync(0xffffffffu, bs, off);
-      const float ol = __shfl_xor_sync(0xffffffffu, bl, off);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (os > bs || (os == bs && oi < bi)) {
-        bs = os;
-        bl = ol;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const int bi = static_cast<int>(__reduce_min_sync(0xffffffffu, bk == m && m != 0u
+                                                                        ? static_cast<uint32_t>(lane + 32 * bs)
+                                                                        : 0xFFFFFFFFu));
+    const float wl = __shfl_sync(0xffffffffu, bl, bi & 31);
+    if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
-      my_l = bl;
+      my_l = wl;
       my_i = bi;
     }
   }
